@@ -1,0 +1,271 @@
+/*
+ * CPU oracle for the GLM MoE feed-forward sublayer forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY: loaded by the tests, the smoke check and the
+ * benchmark's CPU-baseline leg, never by the product path.  Plain loops in
+ * the order the definitions state them, fp64 accumulation, OpenMP over
+ * tokens (tokens are independent).  See moe_oracle.h for the step list and
+ * the passages each step follows.
+ */
+#include "moe_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---- storage access ------------------------------------------------------ */
+
+/* Element i of a tensor stored as fp32 (dtype 0) or bf16 bit patterns (dtype 1). */
+static inline float get(const void* p, int64_t i, int dtype) {
+    if (dtype == 0) return ((const float*)p)[i];
+    uint32_t bits = (uint32_t)((const uint16_t*)p)[i] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return f;
+}
+
+/* Round an fp32 value to the nearest bf16 value, ties to even (the rounding
+ * torch uses for .to(torch.bfloat16)).  Inputs are finite in this oracle. */
+static inline float round_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    u &= 0xffff0000u;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static inline double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* ---- step A: RMSNorm (GlmMoeDsaRMSNorm.forward) --------------------------- */
+
+static void rmsnorm_row(const oracle_cfg* c, const void* x, int64_t row, const void* gain,
+                        float* xn) {
+    const int d = c->d;
+    /* hidden_states.to(float32).pow(2).mean(-1): the exact mean, rounded to fp32 */
+    double ss = 0.0;
+    for (int j = 0; j < d; ++j) {
+        double v = (double)get(x, row * d + j, c->dtype);
+        ss += v * v;
+    }
+    float variance = (float)(ss / (double)d);
+    /* torch.rsqrt(variance + eps): fp32 add, then 1/sqrt as two rounded fp32 ops */
+    float denom = variance + c->eps;
+    float r = 1.0f / sqrtf(denom);
+    for (int j = 0; j < d; ++j) {
+        float n = get(x, row * d + j, c->dtype) * r;      /* fp32 product */
+        float g = get(gain, j, c->dtype);
+        if (c->dtype == 1) {
+            n = round_bf16(n);                             /* .to(input_dtype) */
+            xn[j] = round_bf16(g * n);                     /* weight * hidden, bf16 result */
+        } else {
+            xn[j] = g * n;
+        }
+    }
+}
+
+int oracle_rmsnorm(const oracle_cfg* c, int64_t n, const void* x, const void* gain, float* xn) {
+    if (!c || !x || !gain || !xn || n < 0) return 1;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) rmsnorm_row(c, x, t, gain, xn + t * c->d);
+    return 0;
+}
+
+/* ---- steps B-D: router, selection, weights -------------------------------- */
+
+/* scratch: s [E], b [E], picked [E] (as char) */
+static void route_row(const oracle_cfg* c, const float* xn, const void* Wr, const float* bias,
+                      const int32_t* forced, float* logits, int32_t* idx, float* w,
+                      float* margin, float* s, float* b, char* picked) {
+    const int d = c->d, E = c->E, k = c->k;
+    for (int e = 0; e < E; ++e) {
+        double acc = 0.0;
+        for (int j = 0; j < d; ++j) acc += (double)xn[j] * (double)get(Wr, (int64_t)e * d + j, c->dtype);
+        float l = (float)acc;                              /* fp32 router logit */
+        if (logits) logits[e] = l;
+        s[e] = (float)(1.0 / (1.0 + exp(-(double)l)));     /* sigmoid, rounded to fp32 */
+        b[e] = s[e] + bias[e];                             /* biased score, fp32 add */
+        picked[e] = 0;
+    }
+    /* top-k of b: repeatedly take the largest remaining; on equal values the
+     * first (lowest) index found wins because only a strictly larger value
+     * replaces the current best. */
+    for (int j = 0; j < k; ++j) {
+        int best = -1;
+        if (forced) {
+            best = forced[j];
+        } else {
+            for (int e = 0; e < E; ++e) {
+                if (picked[e]) continue;
+                if (best < 0 || b[e] > b[best]) best = e;
+            }
+        }
+        picked[best] = 1;
+        idx[j] = best;
+    }
+    if (margin) {
+        float next = -INFINITY;
+        int any = 0;
+        for (int e = 0; e < E; ++e)
+            if (!picked[e] && (!any || b[e] > next)) { next = b[e]; any = 1; }
+        margin[0] = any ? b[idx[k - 1]] - next : INFINITY;
+    }
+    /* weights: unbiased sigmoids of the chosen experts, renormalised, scaled */
+    double ssum = 0.0;
+    for (int j = 0; j < k; ++j) ssum += (double)s[idx[j]];
+    for (int j = 0; j < k; ++j)
+        w[j] = (float)((double)c->routed_scale * (double)s[idx[j]] / ssum);
+}
+
+int oracle_route(const oracle_cfg* c, int64_t n, const float* xn, const void* router_w,
+                 const float* corr_bias, float* logits, int32_t* idx, float* w, float* margin) {
+    if (!c || !xn || !router_w || !corr_bias || n < 0 || c->k < 1 || c->k > c->E) return 1;
+    int failed = 0;
+#pragma omp parallel
+    {
+        float* s = (float*)malloc(sizeof(float) * c->E);
+        float* b = (float*)malloc(sizeof(float) * c->E);
+        char* picked = (char*)malloc(c->E);
+        int32_t* idx_t = (int32_t*)malloc(sizeof(int32_t) * c->k);
+        float* w_t = (float*)malloc(sizeof(float) * c->k);
+        if (!s || !b || !picked || !idx_t || !w_t) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int64_t t = 0; t < n; ++t) {
+                route_row(c, xn + t * c->d, router_w, corr_bias, NULL,
+                          logits ? logits + t * c->E : NULL, idx_t, w_t,
+                          margin ? margin + t : NULL, s, b, picked);
+                for (int j = 0; j < c->k; ++j) {
+                    if (idx) idx[t * c->k + j] = idx_t[j];
+                    if (w) w[t * c->k + j] = w_t[j];
+                }
+            }
+        }
+        free(s); free(b); free(picked); free(idx_t); free(w_t);
+    }
+    return failed ? 2 : 0;
+}
+
+/* ---- steps E-I: experts, shared expert, combine --------------------------- */
+
+/* One SwiGLU expert in the grouped layout: gu [d, 2I] (gate cols 0..I-1,
+ * up cols I..2I-1), dn [I, d].  Adds w * y into acc [d].
+ * scratch: g [I], u [I] (double) */
+static void routed_expert(const oracle_cfg* c, const float* xn, const void* gu, const void* dn,
+                          int64_t gu_off, int64_t dn_off, double wgt, double* acc,
+                          double* g, double* u) {
+    const int d = c->d, I = c->I;
+    for (int i = 0; i < I; ++i) { g[i] = 0.0; u[i] = 0.0; }
+    for (int j = 0; j < d; ++j) {
+        double xj = (double)xn[j];
+        int64_t rowb = gu_off + (int64_t)j * 2 * I;
+        for (int i = 0; i < I; ++i) {
+            g[i] += xj * (double)get(gu, rowb + i, c->dtype);
+            u[i] += xj * (double)get(gu, rowb + I + i, c->dtype);
+        }
+    }
+    for (int i = 0; i < I; ++i) g[i] = silu(g[i]) * u[i];  /* h */
+    for (int i = 0; i < I; ++i) {
+        double hw = wgt * g[i];
+        int64_t rowb = dn_off + (int64_t)i * d;
+        for (int o = 0; o < d; ++o) acc[o] += hw * (double)get(dn, rowb + o, c->dtype);
+    }
+}
+
+/* Shared expert with nn.Linear weights: Gs, Us [Is, d], Ds [d, Is].  Adds sh into acc. */
+static void shared_expert(const oracle_cfg* c, const float* xn, const void* Gs, const void* Us,
+                          const void* Ds, double* acc, double* h) {
+    const int d = c->d, Is = c->Is;
+    for (int i = 0; i < Is; ++i) {
+        double gs = 0.0, us = 0.0;
+        for (int j = 0; j < d; ++j) {
+            gs += (double)get(Gs, (int64_t)i * d + j, c->dtype) * (double)xn[j];
+            us += (double)get(Us, (int64_t)i * d + j, c->dtype) * (double)xn[j];
+        }
+        h[i] = silu(gs) * us;
+    }
+    for (int o = 0; o < d; ++o) {
+        double v = 0.0;
+        for (int i = 0; i < Is; ++i) v += (double)get(Ds, (int64_t)o * Is + i, c->dtype) * h[i];
+        acc[o] += v;
+    }
+}
+
+int oracle_forward(const oracle_cfg* c, int64_t n, const int64_t* rows,
+                   const void* x, const void* gain, const void* router_w, const float* corr_bias,
+                   const void* gate_up, const void* down,
+                   const void* shared_gate, const void* shared_up, const void* shared_down,
+                   const int32_t* forced_idx,
+                   float* out, int32_t* idx, float* w, float* margin, float* xn_out,
+                   float* logits) {
+    if (!c || !x || !gain || !router_w || !corr_bias || !gate_up || !down || !out || n < 0)
+        return 1;
+    if (c->k < 1 || c->k > c->E || c->d < 1 || c->I < 1 || c->Is < 0) return 1;
+    if (c->Is > 0 && (!shared_gate || !shared_up || !shared_down)) return 1;
+    const int d = c->d, E = c->E, I = c->I, k = c->k;
+    int failed = 0;
+#pragma omp parallel
+    {
+        int hmax = I > c->Is ? I : c->Is;
+        float* xn = (float*)malloc(sizeof(float) * d);
+        float* s = (float*)malloc(sizeof(float) * E);
+        float* b = (float*)malloc(sizeof(float) * E);
+        char* picked = (char*)malloc(E);
+        int32_t* sel = (int32_t*)malloc(sizeof(int32_t) * k);
+        float* wt = (float*)malloc(sizeof(float) * k);
+        double* acc = (double*)malloc(sizeof(double) * d);
+        double* g = (double*)malloc(sizeof(double) * hmax);
+        double* u = (double*)malloc(sizeof(double) * I);
+        if (!xn || !s || !b || !picked || !sel || !wt || !acc || !g || !u) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t t = 0; t < n; ++t) {
+                int64_t row = rows ? rows[t] : t;
+                rmsnorm_row(c, x, row, gain, xn);
+                route_row(c, xn, router_w, corr_bias, forced_idx ? forced_idx + t * k : NULL,
+                          logits ? logits + t * E : NULL, sel, wt,
+                          margin ? margin + t : NULL, s, b, picked);
+                for (int o = 0; o < d; ++o) acc[o] = 0.0;
+                if (c->Is > 0) shared_expert(c, xn, shared_gate, shared_up, shared_down, acc, g);
+                for (int j = 0; j < k; ++j) {
+                    int e = sel[j];
+                    routed_expert(c, xn, gate_up, down, (int64_t)e * d * 2 * I,
+                                  (int64_t)e * I * d, (double)wt[j], acc, g, u);
+                }
+                for (int o = 0; o < d; ++o)
+                    out[t * d + o] = (float)((double)get(x, row * d + o, c->dtype) + acc[o]);
+                for (int j = 0; j < k; ++j) {
+                    if (idx) idx[t * k + j] = sel[j];
+                    if (w) w[t * k + j] = wt[j];
+                }
+                if (xn_out) memcpy(xn_out + t * d, xn, sizeof(float) * d);
+            }
+        }
+        free(xn); free(s); free(b); free(picked); free(sel); free(wt); free(acc); free(g); free(u);
+    }
+    return failed ? 2 : 0;
+}
+
+int64_t oracle_param_count(const oracle_cfg* c) {
+    int64_t d = c->d, E = c->E, I = c->I, Is = c->Is;
+    int64_t routed = E * d * 2 * I + E * I * d;       /* gate_and_up_projs + down_projs */
+    int64_t shared = Is * d + Is * d + d * Is;         /* gate_proj, up_proj, down_proj */
+    int64_t router = E * d + E;                        /* router weight + correction bias */
+    return routed + shared + router;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
