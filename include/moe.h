@@ -1,0 +1,182 @@
+/*
+ * moe.h — C ABI of the B300 (sm_103a) forward pass of the GLM MoE
+ * feed-forward sublayer.
+ *
+ * The operation (per token t; tokens are independent):
+ *   xn  = RMSNorm(x[t]) with one gain per feature: mean of squares in fp32,
+ *         multiply by rsqrt(mean + eps), cast back to the input dtype, then
+ *         multiply by the gain (GlmMoeDsaRMSNorm.forward, GLM-5 shared-expert
+ *         page on OpenModelAtlas).
+ *   l   = xn . router_w^T in fp32; s = sigmoid(l); b = s + corr_bias
+ *         (the correction bias is a per-expert buffer: GLM-5 MoE block page,
+ *         note under the parameter table).
+ *   idx = the top_k experts by b, descending, ties to the lower index.
+ *   w   = routed_scale * s[idx] / sum(s[idx]).
+ *   y_e = SwiGLU expert in the grouped native layout (NeMo AutoModel
+ *         GLM4-MoE state dict adapter page): gate = xn @ gate_up[e][:, :I],
+ *         up = xn @ gate_up[e][:, I:], y_e = (silu(gate) * up) @ down[e]
+ *         (SwiGLU: GlmMoeDsaMLP.forward).
+ *   sh  = shared SwiGLU expert with nn.Linear weights [out, in]:
+ *         shared_down @ (silu(shared_gate @ xn) * (shared_up @ xn)).
+ *   out = x + sh + sum_j w_j * y_{idx_j}   (second residual add of
+ *         GlmMoeDsaDecoderLayer.forward).
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are row-major and contiguous, in the dtype the handle
+ *     was created with (fp32, or bf16 as 16-bit patterns), except corr_bias,
+ *     which is always fp32.  "device" pointers must be CUDA device memory of
+ *     the handle's device; "host" pointers ordinary host memory (pinned
+ *     memory makes the copies asynchronous to the host).
+ *   - The caller owns every tensor it passes and keeps it valid until the
+ *     work queued on `stream` has finished.  The library owns only the
+ *     workspace it allocates in moe_init and frees in moe_destroy.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - Functions return a moe_status and never throw.  Argument errors are
+ *     detected on the host before any work is queued.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_handle moe_handle;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, aliasing output */
+    MOE_ERR_UNSUPPORTED = 2,  /* valid, but a shape this build does not handle */
+    MOE_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
+    MOE_ERR_OOM = 4,          /* workspace allocation failed in moe_init */
+    MOE_ERR_TIMEOUT = 5       /* a kernel's bounded wait expired (device error flag) */
+} moe_status;
+
+typedef enum { MOE_DTYPE_FP32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
+
+typedef struct {
+    int32_t max_tokens;    /* largest T a forward may use (workspace sizing), >= 1 */
+    int32_t hidden;        /* d */
+    int32_t n_experts;     /* E, 1..1024 */
+    int32_t inter;         /* I, routed expert intermediate size */
+    int32_t shared_inter;  /* Is, shared expert intermediate size; 0 = no shared expert */
+    int32_t max_top_k;     /* largest top_k a forward may use, 1..min(E, 32) */
+    int32_t dtype;         /* moe_dtype of x, weights and out */
+    float eps;             /* RMSNorm epsilon (the pages' default: 1e-6) */
+    int32_t device;        /* CUDA device ordinal */
+    int32_t gemm_path;     /* 0 = automatic (tensor cores for bf16); 1 = force the
+                              CUDA-core (FFMA) expert kernels (the fp32 path) */
+} moe_config;
+
+/* Creates a handle on cfg->device and allocates its workspace for
+ * max_tokens * max_top_k routed rows.  bf16 handles on the tensor-core path
+ * need hidden, inter and shared_inter to be multiples of 64
+ * (MOE_ERR_UNSUPPORTED otherwise).  *out is set only on MOE_OK. */
+MOE_API moe_status moe_init(const moe_config* cfg, moe_handle** out);
+
+/* One forward pass of the sublayer over T tokens (0 <= T <= max_tokens),
+ * queued on `stream`; asynchronous, no host synchronisation, no allocation.
+ * All pointers are device pointers:
+ *   x           [T, d]          input hidden states (the residual)
+ *   norm_w      [d]             RMSNorm gain
+ *   router_w    [E, d]          router weight (logits = xn . router_w^T)
+ *   corr_bias   [E]  fp32       per-expert correction bias (selection only)
+ *   gate_up     [E, d, 2I]      grouped gate|up projections: columns 0..I-1
+ *                               are the gate, I..2I-1 the up projection
+ *   down        [E, I, d]       grouped down projections
+ *   shared_gate [Is, d], shared_up [Is, d], shared_down [d, Is]
+ *                               shared expert (nn.Linear [out, in]); may be
+ *                               NULL when the handle has shared_inter == 0
+ *   top_k       1..max_top_k;  routed_scale: factor on the renormalised weights
+ *   out         [T, d]          must not overlap any input
+ * x, out and the weight tensors must be 16-byte aligned.  T == 0 queues
+ * nothing and reads no pointer (any may be NULL).  A device-side timeout is
+ * reported by moe_sync_status. */
+MOE_API moe_status moe_forward(moe_handle* h, int32_t T, const void* x, const void* norm_w,
+                       const void* router_w, const float* corr_bias, const void* gate_up,
+                       const void* down, const void* shared_gate, const void* shared_up,
+                       const void* shared_down, int32_t top_k, float routed_scale, void* out,
+                       void* stream);
+
+/* moe_forward with x and out in HOST memory (the weights stay device
+ * pointers): copies x into the handle's device staging buffer, runs the
+ * forward, copies the result back into `out` and synchronises `stream`.
+ * Returns MOE_ERR_TIMEOUT if a kernel's bounded wait expired. */
+MOE_API moe_status moe_forward_host(moe_handle* h, int32_t T, const void* x_host, const void* norm_w,
+                            const void* router_w, const float* corr_bias, const void* gate_up,
+                            const void* down, const void* shared_gate, const void* shared_up,
+                            const void* shared_down, int32_t top_k, float routed_scale,
+                            void* out_host, void* stream);
+
+/* Routing of the last forward on this handle, copied (device to device, on
+ * `stream`) into caller buffers; any pointer may be NULL:
+ *   idx [T, top_k] int32 expert ids in slot order, w [T, top_k] fp32 weights,
+ *   counts [E] int32 tokens routed to each expert. */
+MOE_API moe_status moe_get_routing(moe_handle* h, int32_t* idx, float* w, int32_t* counts,
+                           void* stream);
+
+/* Intermediates of the last forward, for stage-by-stage testing. */
+typedef enum {
+    MOE_T_XN = 0,       /* [T, d] RMSNorm output, handle dtype */
+    MOE_T_LOGITS = 1,   /* [T, E] fp32 router logits */
+    MOE_T_OFFSETS = 2,  /* [E + 1] int32 first permuted row of each expert */
+    MOE_T_POS = 3,      /* [T, top_k] int32 permuted row of each (token, slot) */
+    MOE_T_ROW_TOK = 4,  /* [T * top_k] int32 token of each permuted row */
+    MOE_T_H = 5,        /* [T * top_k, I] routed SwiGLU activations, handle dtype */
+    MOE_T_SHARED = 6    /* [T, d] shared expert output, handle dtype */
+} moe_tensor;
+
+/* Copies intermediate `which` of the last forward into dst (device memory
+ * of dst_bytes bytes) on `stream`.  MOE_ERR_INVALID_ARG if dst_bytes is
+ * smaller than the tensor. */
+MOE_API moe_status moe_get_intermediate(moe_handle* h, moe_tensor which, void* dst, size_t dst_bytes,
+                                void* stream);
+
+/* Synchronises `stream`, then reads and clears the handle's device error
+ * flag: MOE_ERR_TIMEOUT if a kernel gave up a bounded wait since the last
+ * call, MOE_ERR_CUDA on an asynchronous CUDA error, else MOE_OK. */
+MOE_API moe_status moe_sync_status(moe_handle* h, void* stream);
+
+/* Counters of the forwards run since the last moe_read_stats. */
+#define MOE_MAX_STAGES 16
+typedef struct {
+    int32_t forwards;                /* forwards counted */
+    int32_t launches;                /* kernels those forwards launched */
+    int32_t n_stages;                /* stages of the forward (entries of stage_ms in use) */
+    float stage_ms[MOE_MAX_STAGES];  /* summed GPU time per stage, from CUDA events recorded on
+                                        the forward's stream while profiling is on; else 0.
+                                        Stages: 0 RMSNorm (fused with the router on the
+                                        CUDA-core path), 1 router logits, 2 top-k, 3 scan,
+                                        4 scatter, 5 row gather, 6 gate|up + SwiGLU (routed and
+                                        shared), 7 down + routing weight (routed and shared),
+                                        8 combine + residual. */
+} moe_stats;
+
+/* Turns per-stage CUDA-event timing on (enable != 0) or off.  Recording
+ * events does not synchronise; after 256 profiled forwards without a
+ * moe_read_stats call, the next forward waits for the oldest one. */
+MOE_API moe_status moe_set_profiling(moe_handle* h, int32_t enable);
+
+/* Synchronises the device, returns the counters accumulated since the last
+ * call, and resets them. */
+MOE_API moe_status moe_read_stats(moe_handle* h, moe_stats* out);
+
+/* Frees the workspace (synchronises the device first).  NULL is a no-op. */
+MOE_API moe_status moe_destroy(moe_handle* h);
+
+/* Static description of a status code. */
+MOE_API const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

@@ -1,0 +1,189 @@
+"""Thin Python binding of the C ABI in include/moe.h (ctypes).
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+kernels of libmoe_b300.so.  PyTorch is used for device memory and streams.
+Loading fails loudly when the library has not been built; there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmoe_b300.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_OOM, MOE_ERR_TIMEOUT = range(6)
+DTYPE_FP32, DTYPE_BF16 = 0, 1
+T_XN, T_LOGITS, T_OFFSETS, T_POS, T_ROW_TOK, T_H, T_SHARED = range(7)
+
+# Functions the header declares (kept in sync by the ABI test).
+EXPORTS = ("moe_init", "moe_forward", "moe_forward_host", "moe_get_routing",
+           "moe_get_intermediate", "moe_sync_status", "moe_set_profiling", "moe_read_stats",
+           "moe_destroy", "moe_status_string")
+STAGES = ("rmsnorm", "router", "topk", "scan", "scatter", "gather", "gate_up_swiglu",
+          "down_weighted", "combine")
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("max_tokens", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("n_experts", ctypes.c_int32), ("inter", ctypes.c_int32),
+                ("shared_inter", ctypes.c_int32), ("max_top_k", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("eps", ctypes.c_float),
+                ("device", ctypes.c_int32), ("gemm_path", ctypes.c_int32)]
+
+
+class MoeStats(ctypes.Structure):
+    _fields_ = [("forwards", ctypes.c_int32), ("launches", ctypes.c_int32),
+                ("n_stages", ctypes.c_int32), ("stage_ms", ctypes.c_float * 16)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libmoe_b300.so and declares the signatures.  Raises if missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "`python -m mixture_experts_transformer_sigmoid_b300.build`")
+    lib = ctypes.CDLL(path)
+    P, I32, F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+    lib.moe_init.argtypes = [ctypes.POINTER(MoeConfig), ctypes.POINTER(ctypes.c_void_p)]
+    fwd = [P, I32, P, P, P, P, P, P, P, P, P, I32, F32, P, P]
+    lib.moe_forward.argtypes = fwd
+    lib.moe_forward_host.argtypes = fwd
+    lib.moe_get_routing.argtypes = [P, P, P, P, P]
+    lib.moe_get_intermediate.argtypes = [P, ctypes.c_int, P, ctypes.c_size_t, P]
+    lib.moe_sync_status.argtypes = [P, P]
+    lib.moe_set_profiling.argtypes = [P, I32]
+    lib.moe_read_stats.argtypes = [P, ctypes.POINTER(MoeStats)]
+    lib.moe_destroy.argtypes = [P]
+    lib.moe_status_string.argtypes = [ctypes.c_int]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    for name in EXPORTS[:-1]:
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().moe_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class MoeSublayer:
+    """One handle of the C ABI: workspace for up to ``max_tokens`` tokens."""
+
+    def __init__(self, *, max_tokens: int, hidden: int, n_experts: int, inter: int,
+                 shared_inter: int, max_top_k: int, dtype: str = "bf16", eps: float = 1e-6,
+                 device: int = 0, gemm_path: int = 0):
+        self.lib = load_library()
+        self.cfg = MoeConfig(max_tokens, hidden, n_experts, inter, shared_inter, max_top_k,
+                             DTYPE_BF16 if dtype == "bf16" else DTYPE_FP32, eps, device, gemm_path)
+        self.dtype = torch.bfloat16 if dtype == "bf16" else torch.float32
+        self.device = torch.device("cuda", device)
+        h = ctypes.c_void_p()
+        _check(self.lib.moe_init(ctypes.byref(self.cfg), ctypes.byref(h)), "moe_init")
+        self.handle = h
+        self.last_T = 0
+        self.last_k = 0
+
+    def close(self):
+        if self.handle is not None and self.handle.value:
+            self.lib.moe_destroy(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _stream(stream):
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        return ctypes.c_void_p(stream.cuda_stream)
+
+    def forward(self, x, w: dict, top_k: int, routed_scale: float, out=None, stream=None):
+        """x [T, d] on the device; w holds norm_w, router_w, corr_bias,
+        gate_up, down, shared_gate, shared_up, shared_down (device tensors)."""
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty_like(x)
+        st = self._stream(stream)
+        _check(self.lib.moe_forward(
+            self.handle, T, _ptr(x), _ptr(w["norm_w"]), _ptr(w["router_w"]), _ptr(w["corr_bias"]),
+            _ptr(w["gate_up"]), _ptr(w["down"]), _ptr(w.get("shared_gate")),
+            _ptr(w.get("shared_up")), _ptr(w.get("shared_down")), top_k, routed_scale,
+            _ptr(out), st), "moe_forward")
+        self.last_T, self.last_k = T, top_k
+        return out
+
+    def forward_host(self, x_host, w: dict, top_k: int, routed_scale: float, out_host,
+                     stream=None):
+        """x_host / out_host: CPU tensors (pinned for asynchronous copies)."""
+        T = x_host.shape[0]
+        _check(self.lib.moe_forward_host(
+            self.handle, T, _ptr(x_host), _ptr(w["norm_w"]), _ptr(w["router_w"]),
+            _ptr(w["corr_bias"]), _ptr(w["gate_up"]), _ptr(w["down"]),
+            _ptr(w.get("shared_gate")), _ptr(w.get("shared_up")), _ptr(w.get("shared_down")),
+            top_k, routed_scale, _ptr(out_host), self._stream(stream)), "moe_forward_host")
+        self.last_T, self.last_k = T, top_k
+        return out_host
+
+    def routing(self, stream=None):
+        T, k, E = self.last_T, self.last_k, self.cfg.n_experts
+        idx = torch.empty((T, k), dtype=torch.int32, device=self.device)
+        wt = torch.empty((T, k), dtype=torch.float32, device=self.device)
+        counts = torch.empty((E,), dtype=torch.int32, device=self.device)
+        _check(self.lib.moe_get_routing(self.handle, _ptr(idx), _ptr(wt), _ptr(counts),
+                                        self._stream(stream)), "moe_get_routing")
+        return idx, wt, counts
+
+    def intermediate(self, which: int, stream=None):
+        T, k, c = self.last_T, self.last_k, self.cfg
+        shapes = {T_XN: ((T, c.hidden), self.dtype), T_LOGITS: ((T, c.n_experts), torch.float32),
+                  T_OFFSETS: ((c.n_experts + 1,), torch.int32), T_POS: ((T, k), torch.int32),
+                  T_ROW_TOK: ((T * k,), torch.int32), T_H: ((T * k, c.inter), self.dtype),
+                  T_SHARED: ((T, c.hidden), self.dtype)}
+        shape, dt = shapes[which]
+        dst = torch.empty(shape, dtype=dt, device=self.device)
+        _check(self.lib.moe_get_intermediate(self.handle, which, _ptr(dst),
+                                             dst.numel() * dst.element_size(),
+                                             self._stream(stream)), "moe_get_intermediate")
+        return dst
+
+    def sync_status(self, stream=None) -> int:
+        return self.lib.moe_sync_status(self.handle, self._stream(stream))
+
+    def set_profiling(self, enable: bool):
+        _check(self.lib.moe_set_profiling(self.handle, 1 if enable else 0), "moe_set_profiling")
+
+    def read_stats(self) -> dict:
+        """Counters since the last call: forwards, kernel launches, and the
+        summed GPU milliseconds of each stage (profiling on)."""
+        st = MoeStats()
+        _check(self.lib.moe_read_stats(self.handle, ctypes.byref(st)), "moe_read_stats")
+        return {"forwards": st.forwards, "launches": st.launches,
+                "stage_ms": {STAGES[i]: float(st.stage_ms[i]) for i in range(st.n_stages)}}

@@ -1,0 +1,463 @@
+// CUDA-core kernels of the MoE sublayer: RMSNorm, router logits (FFMA
+// path), per-token top-k, the expert histogram / scan / stable scatter that
+// build the permuted row index, the row gather, the deterministic combine,
+// and the FFMA expert kernels used for fp32 storage.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace moe {
+
+constexpr int CHUNK_TOKENS = 128;  // tokens per histogram chunk (topk and scatter agree on it)
+
+// ------------------------------------------------------------ element I/O
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int V = 4;  // elements per 16-byte vector
+    __device__ static float to_f(float v) { return v; }
+    __device__ static float from_f(float v) { return v; }
+    // RMSNorm's cast back to the input dtype is the identity for fp32
+    __device__ static float round_io(float v) { return v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int V = 8;
+    __device__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    __device__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+    __device__ static float round_io(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+};
+
+template <typename T>
+__device__ __forceinline__ void load_vec(const T* p, float (&f)[Elem<T>::V]) {
+    int4 raw = *reinterpret_cast<const int4*>(p);
+    const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+    for (int i = 0; i < Elem<T>::V; ++i) f[i] = Elem<T>::to_f(e[i]);
+}
+template <typename T>
+__device__ __forceinline__ void store_vec(T* p, const float (&f)[Elem<T>::V]) {
+    int4 raw;
+    T* e = reinterpret_cast<T*>(&raw);
+#pragma unroll
+    for (int i = 0; i < Elem<T>::V; ++i) e[i] = Elem<T>::from_f(f[i]);
+    *reinterpret_cast<int4*>(p) = raw;
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+// --------------------------------------------------------------- RMSNorm
+// Error-free addition (Knuth's two-sum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// Block-wide sum of (hi, lo) pairs; every thread receives the total.
+__device__ __forceinline__ void block_sum_pair(float& hi, float& lo, float2* red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        float oh = __shfl_xor_sync(0xffffffffu, hi, off);
+        float ol = __shfl_xor_sync(0xffffffffu, lo, off);
+        float s, e;
+        two_sum(hi, oh, s, e);
+        hi = s;
+        lo = __fadd_rn(__fadd_rn(lo, ol), e);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    if (lane == 0) red[warp] = make_float2(hi, lo);
+    __syncthreads();
+    if (warp == 0) {
+        float2 v = lane < nw ? red[lane] : make_float2(0.f, 0.f);
+        hi = v.x;
+        lo = v.y;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            float oh = __shfl_xor_sync(0xffffffffu, hi, off);
+            float ol = __shfl_xor_sync(0xffffffffu, lo, off);
+            float s, e;
+            two_sum(hi, oh, s, e);
+            hi = s;
+            lo = __fadd_rn(__fadd_rn(lo, ol), e);
+        }
+        if (lane == 0) red[32] = make_float2(hi, lo);
+    }
+    __syncthreads();
+    hi = red[32].x;
+    lo = red[32].y;
+}
+
+// Reciprocal RMS of one row (GlmMoeDsaRMSNorm.forward): the mean of squares
+// is accumulated with compensated fp32 sums (squares split exactly with an
+// FMA), so it equals the exact mean rounded to fp32 except in vanishingly
+// rare cases; then rsqrt(mean + eps) as an fp32 add, sqrt and divide, each
+// correctly rounded.
+template <typename T>
+__device__ __forceinline__ float row_rrms(const T* xr, int d, float eps, float2* red) {
+    constexpr int V = Elem<T>::V;
+    float hi = 0.f, lo = 0.f;
+    for (int v = threadIdx.x; v < d / V; v += blockDim.x) {
+        float f[V];
+        load_vec<T>(xr + v * V, f);
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            float p = __fmul_rn(f[i], f[i]);
+            float pe = fmaf(f[i], f[i], -p);  // exact low part of the square
+            float s, e;
+            two_sum(hi, p, s, e);
+            hi = s;
+            lo = __fadd_rn(lo, __fadd_rn(e, pe));
+        }
+    }
+    block_sum_pair(hi, lo, red);
+    const float ms = static_cast<float>((static_cast<double>(hi) + static_cast<double>(lo)) /
+                                        static_cast<double>(d));
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+// xn = gain * cast(x * r): one block per token.
+template <typename T>
+__global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ gain,
+                               T* __restrict__ xn, int d, float eps) {
+    __shared__ float2 red[33];
+    constexpr int V = Elem<T>::V;
+    const size_t t = blockIdx.x;
+    const T* xr = x + t * d;
+    const float r = row_rrms<T>(xr, d, eps, red);
+    for (int v = threadIdx.x; v < d / V; v += blockDim.x) {
+        float f[V], g[V];
+        load_vec<T>(xr + v * V, f);
+        load_vec<T>(gain + v * V, g);
+#pragma unroll
+        for (int i = 0; i < V; ++i) f[i] = __fmul_rn(g[i], Elem<T>::round_io(__fmul_rn(f[i], r)));
+        store_vec<T>(xn + t * d + v * V, f);
+    }
+}
+
+// RMSNorm fused with the router logits on CUDA cores (fp32 accumulation):
+// one block per token; the normalised row stays in shared memory and each
+// warp takes experts e = warp, warp + nwarps, ... with 16-byte loads of the
+// router weight and a warp-shuffle reduction.  Dynamic smem: d floats.
+template <typename T>
+__global__ void rmsnorm_router_kernel(const T* __restrict__ x, const T* __restrict__ gain,
+                                      const T* __restrict__ router_w, T* __restrict__ xn,
+                                      float* __restrict__ logits, int d, int E, float eps) {
+    extern __shared__ float xs[];
+    __shared__ float2 red[33];
+    constexpr int V = Elem<T>::V;
+    const size_t t = blockIdx.x;
+    const T* xr = x + t * d;
+    const float r = row_rrms<T>(xr, d, eps, red);
+    for (int v = threadIdx.x; v < d / V; v += blockDim.x) {
+        float f[V], g[V];
+        load_vec<T>(xr + v * V, f);
+        load_vec<T>(gain + v * V, g);
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            f[i] = __fmul_rn(g[i], Elem<T>::round_io(__fmul_rn(f[i], r)));
+            f[i] = Elem<T>::round_io(f[i]);
+            xs[v * V + i] = f[i];
+        }
+        store_vec<T>(xn + t * d + v * V, f);
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int e = warp; e < E; e += nw) {
+        const T* wr = router_w + static_cast<size_t>(e) * d;
+        float acc = 0.f;
+        for (int v = lane; v < d / V; v += 32) {
+            float w[V];
+            load_vec<T>(wr + v * V, w);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc = fmaf(xs[v * V + i], w[i], acc);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) logits[t * E + e] = acc;
+    }
+}
+
+// ------------------------------------------------------------------ top-k
+// One warp per token.  s = sigmoid(l), b = s + bias; k rounds of a warp
+// argmax on (b descending, expert index ascending); slot j's expert and
+// sigmoid end up in lane j.  w_j = routed_scale * s_j / sum_i s_i.  Each
+// block covers CHUNK_TOKENS tokens and writes that chunk's expert histogram.
+// EPL = experts per lane (ceil(E / 32)).
+template <int EPL>
+__global__ void topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+                            int T, int E, int k, float routed_scale, int* __restrict__ idx_out,
+                            float* __restrict__ w_out, int* __restrict__ chunk_cnt) {
+    extern __shared__ int cnt[];  // [E]
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int chunk = blockIdx.x;
+    for (int tl = warp; tl < CHUNK_TOKENS; tl += nw) {
+        const int t = chunk * CHUNK_TOKENS + tl;
+        if (t >= T) break;
+        float bv[EPL], sv[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) {
+                const float l = logits[static_cast<size_t>(t) * E + e];
+                const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
+                const float b = __fadd_rn(s, bias[e]);
+                sv[i] = s;
+                bv[i] = (b == b) ? b : -INFINITY;  // a NaN score ranks last (keeps the order total)
+            } else {
+                sv[i] = 0.f;
+                bv[i] = 0.f;
+            }
+        }
+        int my_e = 0;
+        float my_s = 0.f;
+        uint32_t removed = 0u;  // bit i: expert lane + 32 i already selected
+        for (int j = 0; j < k; ++j) {
+            // candidate of this lane: the best unselected expert it holds; every
+            // unselected expert is a candidate, so a winner always exists (k <= E)
+            float bb = 0.f, bs = 0.f;
+            int be = -1;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E && !((removed >> i) & 1u) && (be < 0 || bv[i] > bb)) {
+                    bb = bv[i];
+                    be = e;
+                    bs = sv[i];
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ob = __shfl_xor_sync(0xffffffffu, bb, off);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+                const float os = __shfl_xor_sync(0xffffffffu, bs, off);
+                if (oe >= 0 && (be < 0 || ob > bb || (ob == bb && oe < be))) {
+                    bb = ob;
+                    be = oe;
+                    bs = os;
+                }
+            }
+            if ((be & 31) == lane) removed |= 1u << (be >> 5);
+            if (lane == j) { my_e = be; my_s = bs; }
+        }
+        float ssum = 0.f;
+        for (int j = 0; j < k; ++j) ssum = __fadd_rn(ssum, __shfl_sync(0xffffffffu, my_s, j));
+        if (lane < k) {
+            idx_out[static_cast<size_t>(t) * k + lane] = my_e;
+            w_out[static_cast<size_t>(t) * k + lane] =
+                __fdiv_rn(__fmul_rn(routed_scale, my_s), ssum);
+            atomicAdd(&cnt[my_e], 1);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        chunk_cnt[static_cast<size_t>(chunk) * E + e] = cnt[e];
+}
+
+// --------------------------------------------------- histogram scan (1 block)
+// counts[e] = sum over chunks; offsets = exclusive scan of counts (offsets[E]
+// = T*k); chunk_base[c][e] = offsets[e] + rows of expert e in chunks < c.
+__global__ void scan_kernel(const int* __restrict__ chunk_cnt, int n_chunks, int E,
+                            int* __restrict__ counts, int* __restrict__ offsets,
+                            int* __restrict__ chunk_base) {
+    __shared__ int warp_tot[32];
+    const int e = threadIdx.x;  // blockDim.x >= E, multiple of 32
+    int total = 0;
+    if (e < E)
+        for (int c = 0; c < n_chunks; ++c) total += chunk_cnt[static_cast<size_t>(c) * E + e];
+    const int lane = e & 31, warp = e >> 5;
+    int incl = total;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += u;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = lane < (blockDim.x >> 5) ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += u;
+        }
+        warp_tot[lane] = v;  // inclusive scan of warp totals
+    }
+    __syncthreads();
+    const int excl = incl - total + (warp > 0 ? warp_tot[warp - 1] : 0);
+    if (e < E) {
+        counts[e] = total;
+        offsets[e] = excl;
+        if (e == E - 1) offsets[E] = excl + total;
+        int run = excl;
+        for (int c = 0; c < n_chunks; ++c) {
+            chunk_base[static_cast<size_t>(c) * E + e] = run;
+            run += chunk_cnt[static_cast<size_t>(c) * E + e];
+        }
+    }
+}
+
+// ---------------------------------------------------------- stable scatter
+// One block (CHUNK_TOKENS threads) per chunk.  The row of (token t, slot j)
+// is chunk_base[c][e] + (number of earlier tokens of the chunk routed to e),
+// so rows of each expert are ordered by token.  Dynamic smem: E * 4 words.
+__global__ void scatter_kernel(const int* __restrict__ idx, const float* __restrict__ w, int T,
+                               int E, int k, const int* __restrict__ chunk_base,
+                               int* __restrict__ pos, int* __restrict__ row_tok,
+                               float* __restrict__ row_w) {
+    extern __shared__ uint32_t mask[];  // [E][CHUNK_TOKENS / 32]
+    constexpr int WORDS = CHUNK_TOKENS / 32;
+    for (int i = threadIdx.x; i < E * WORDS; i += blockDim.x) mask[i] = 0u;
+    __syncthreads();
+    const int tl = threadIdx.x;
+    const int t = blockIdx.x * CHUNK_TOKENS + tl;
+    const bool valid = t < T;
+    if (valid)
+        for (int j = 0; j < k; ++j)
+            atomicOr(&mask[idx[static_cast<size_t>(t) * k + j] * WORDS + (tl >> 5)],
+                     1u << (tl & 31));
+    __syncthreads();
+    if (!valid) return;
+    for (int j = 0; j < k; ++j) {
+        const int e = idx[static_cast<size_t>(t) * k + j];
+        int rank = __popc(mask[e * WORDS + (tl >> 5)] & ((1u << (tl & 31)) - 1u));
+        for (int wi = 0; wi < (tl >> 5); ++wi) rank += __popc(mask[e * WORDS + wi]);
+        const int row = chunk_base[static_cast<size_t>(blockIdx.x) * E + e] + rank;
+        pos[static_cast<size_t>(t) * k + j] = row;
+        row_tok[row] = t;
+        row_w[row] = w[static_cast<size_t>(t) * k + j];
+    }
+}
+
+// xp[row] = xn[row_tok[row]]: one warp per row, 16-byte vectors.  The token
+// index is clamped into [0, n_tok) so that no input can make it read out of range.
+template <typename T>
+__global__ void gather_rows_kernel(const T* __restrict__ xn, const int* __restrict__ row_tok,
+                                   T* __restrict__ xp, int P, int d, int n_tok) {
+    const int lane = threadIdx.x & 31;
+    const int nvec = d * static_cast<int>(sizeof(T)) / 16;
+    for (int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < P;
+         row += (gridDim.x * blockDim.x) >> 5) {
+        const int t = min(max(row_tok[row], 0), n_tok - 1);
+        const int4* src = reinterpret_cast<const int4*>(xn + static_cast<size_t>(t) * d);
+        int4* dst = reinterpret_cast<int4*>(xp + static_cast<size_t>(row) * d);
+        for (int v = lane; v < nvec; v += 32) dst[v] = src[v];
+    }
+}
+
+// out[t] = x[t] + sh[t] + sum_j yp[pos[t, j]] in fp32, slots in order, one
+// rounding at the end (yp rows already carry their routing weight).
+template <typename T>
+__global__ void combine_kernel(const T* __restrict__ x, const T* __restrict__ sh,
+                               const T* __restrict__ yp, const int* __restrict__ pos, int d, int k,
+                               T* __restrict__ out) {
+    constexpr int V = Elem<T>::V;
+    const size_t t = blockIdx.x;
+    for (int v = threadIdx.x; v < d / V; v += blockDim.x) {
+        float acc[V], tmp[V];
+        load_vec<T>(x + t * d + v * V, acc);
+        if (sh != nullptr) {
+            load_vec<T>(sh + t * d + v * V, tmp);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] += tmp[i];
+        }
+        for (int j = 0; j < k; ++j) {
+            const size_t row = static_cast<size_t>(pos[t * k + j]);
+            load_vec<T>(yp + row * d + v * V, tmp);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] += tmp[i];
+        }
+        store_vec<T>(out + t * d + v * V, acc);
+    }
+}
+
+// ------------------------------------------------- FFMA expert kernels (fp32)
+// Expert of a permuted row: the last e with offsets[e] <= row.
+__device__ __forceinline__ int expert_of_row(const int* offsets, int E, int row) {
+    int lo = 0, hi = E;  // offsets[lo] <= row < offsets[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (offsets[mid] <= row) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// h[row, i] = silu(xp[row] . gate_up[e][:, i]) * (xp[row] . gate_up[e][:, I + i]).
+// grid (P, ceil(I / blockDim)); dynamic smem: d floats.
+template <typename T>
+__global__ void simt_gate_up_kernel(const T* __restrict__ xp, const T* __restrict__ gate_up,
+                                    const int* __restrict__ offsets, int E, int d, int I,
+                                    T* __restrict__ h) {
+    extern __shared__ float rowv[];
+    const int row = blockIdx.x;
+    const int e = expert_of_row(offsets, E, row);
+    for (int j = threadIdx.x; j < d; j += blockDim.x)
+        rowv[j] = Elem<T>::to_f(xp[static_cast<size_t>(row) * d + j]);
+    __syncthreads();
+    const int i = blockIdx.y * blockDim.x + threadIdx.x;
+    if (i >= I) return;
+    const T* w = gate_up + static_cast<size_t>(e) * d * 2 * I;
+    float g = 0.f, u = 0.f;
+    for (int j = 0; j < d; ++j) {
+        g = fmaf(rowv[j], Elem<T>::to_f(w[static_cast<size_t>(j) * 2 * I + i]), g);
+        u = fmaf(rowv[j], Elem<T>::to_f(w[static_cast<size_t>(j) * 2 * I + I + i]), u);
+    }
+    h[static_cast<size_t>(row) * I + i] = Elem<T>::from_f(silu_f(g) * u);
+}
+
+// yp[row, o] = row_w[row] * (h[row] . down[e][:, o]).  grid (P, ceil(d / blockDim)).
+template <typename T>
+__global__ void simt_down_kernel(const T* __restrict__ h, const T* __restrict__ down,
+                                 const int* __restrict__ offsets, const float* __restrict__ row_w,
+                                 int E, int I, int d, T* __restrict__ yp) {
+    extern __shared__ float rowv[];
+    const int row = blockIdx.x;
+    const int e = expert_of_row(offsets, E, row);
+    for (int i = threadIdx.x; i < I; i += blockDim.x)
+        rowv[i] = Elem<T>::to_f(h[static_cast<size_t>(row) * I + i]);
+    __syncthreads();
+    const int o = blockIdx.y * blockDim.x + threadIdx.x;
+    if (o >= d) return;
+    const T* w = down + static_cast<size_t>(e) * I * d;
+    float acc = 0.f;
+    for (int i = 0; i < I; ++i) acc = fmaf(rowv[i], Elem<T>::to_f(w[static_cast<size_t>(i) * d + o]), acc);
+    yp[static_cast<size_t>(row) * d + o] = Elem<T>::from_f(acc * row_w[row]);
+}
+
+// Shared expert, nn.Linear weights: hs[t, i] = silu(Gs[i] . xn[t]) * (Us[i] . xn[t]).
+template <typename T>
+__global__ void simt_shared_gate_up_kernel(const T* __restrict__ xn, const T* __restrict__ Gs,
+                                           const T* __restrict__ Us, int d, int Is,
+                                           T* __restrict__ hs) {
+    extern __shared__ float rowv[];
+    const int t = blockIdx.x;
+    for (int j = threadIdx.x; j < d; j += blockDim.x)
+        rowv[j] = Elem<T>::to_f(xn[static_cast<size_t>(t) * d + j]);
+    __syncthreads();
+    const int i = blockIdx.y * blockDim.x + threadIdx.x;
+    if (i >= Is) return;
+    float g = 0.f, u = 0.f;
+    for (int j = 0; j < d; ++j) {
+        g = fmaf(Elem<T>::to_f(Gs[static_cast<size_t>(i) * d + j]), rowv[j], g);
+        u = fmaf(Elem<T>::to_f(Us[static_cast<size_t>(i) * d + j]), rowv[j], u);
+    }
+    hs[static_cast<size_t>(t) * Is + i] = Elem<T>::from_f(silu_f(g) * u);
+}
+
+// sh[t, o] = Ds[o] . hs[t].
+template <typename T>
+__global__ void simt_shared_down_kernel(const T* __restrict__ hs, const T* __restrict__ Ds,
+                                        int Is, int d, T* __restrict__ sh) {
+    extern __shared__ float rowv[];
+    const int t = blockIdx.x;
+    for (int i = threadIdx.x; i < Is; i += blockDim.x)
+        rowv[i] = Elem<T>::to_f(hs[static_cast<size_t>(t) * Is + i]);
+    __syncthreads();
+    const int o = blockIdx.y * blockDim.x + threadIdx.x;
+    if (o >= d) return;
+    float acc = 0.f;
+    for (int i = 0; i < Is; ++i) acc = fmaf(Elem<T>::to_f(Ds[static_cast<size_t>(o) * Is + i]), rowv[i], acc);
+    sh[static_cast<size_t>(t) * d + o] = Elem<T>::from_f(acc);
+}
+
+}  // namespace moe

@@ -1,0 +1,607 @@
+// Host side of the C ABI declared in include/moe.h: argument validation,
+// workspace, TMA tensor-map encoding and the launch sequence of one forward.
+//
+// bf16 forward on one stream (no host synchronisation):
+//   rmsnorm -> router logits (tcgen05 GEMM) -> top-k + chunk histograms ->
+//   scan -> stable scatter -> row gather -> gate|up grouped GEMM with SwiGLU
+//   epilogue (routed experts + shared expert in one launch) -> down grouped
+//   GEMM with routing-weight epilogue (routed + shared in one launch) ->
+//   combine with the residual.
+// fp32 storage (and gemm_path = 1) runs the same routing kernels with the
+// router fused into RMSNorm and the expert contractions on CUDA cores.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <type_traits>
+#include <vector>
+
+#include "k_gemm_tc.cuh"
+#include "k_route.cuh"
+#include "moe.h"
+
+using namespace moe;
+
+struct moe_handle {
+    moe_config cfg;
+    int es;            // bytes per stored element
+    bool tc;           // tensor-core expert/router path
+    int num_sms;
+    int64_t P_max;     // max_tokens * max_top_k
+    int n_chunks_max;
+    // workspace
+    void* xn = nullptr;
+    float* logits = nullptr;
+    int* topk_idx = nullptr;
+    float* topk_w = nullptr;
+    int* chunk_cnt = nullptr;
+    int* chunk_base = nullptr;
+    int* counts = nullptr;
+    int* offsets = nullptr;
+    int* pos = nullptr;
+    int* row_tok = nullptr;
+    float* row_w = nullptr;
+    void* xp = nullptr;
+    void* h = nullptr;
+    void* yp = nullptr;
+    void* hs = nullptr;
+    void* sh = nullptr;
+    void* x_stage = nullptr;
+    void* out_stage = nullptr;
+    int* err = nullptr;
+    int last_T = 0;
+    int last_k = 0;
+    // counters and per-stage profiling (ring of event sets, one per forward)
+    static constexpr int NSTAGE = 9;
+    static constexpr int RING = 256;
+    int64_t launches = 0;
+    int forwards = 0;
+    bool profiling = false;
+    std::vector<cudaEvent_t> ev;  // RING x (NSTAGE + 1)
+    int ring_head = 0, ring_pending = 0;
+    double stage_ms[NSTAGE] = {};
+    cudaEvent_t* cur = nullptr;   // event set of the forward being queued, or null
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+// bf16 tensor [outer][inner] (inner contiguous), 64 x 64 boxes, 128-byte swizzle.
+bool map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// bf16 tensor [groups][mid][inner], 64 x 64 x 1 boxes, 128-byte swizzle.
+bool map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t groups) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {inner, mid, groups};
+    cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
+    cuuint32_t box[3] = {64, 64, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+void free_ws(moe_handle* h) {
+    void* ptrs[] = {h->xn, h->logits, h->topk_idx, h->topk_w, h->chunk_cnt, h->chunk_base,
+                    h->counts, h->offsets, h->pos, h->row_tok, h->row_w, h->xp, h->h, h->yp,
+                    h->hs, h->sh, h->x_stage, h->out_stage, h->err};
+    for (void* p : ptrs)
+        if (p) cudaFree(p);
+}
+
+// Adds the stage times of the oldest pending profiled forward.
+bool fold_oldest(moe_handle* h) {
+    const int slot = (h->ring_head - h->ring_pending + moe_handle::RING) % moe_handle::RING;
+    cudaEvent_t* e = &h->ev[static_cast<size_t>(slot) * (moe_handle::NSTAGE + 1)];
+    if (cudaEventSynchronize(e[moe_handle::NSTAGE]) != cudaSuccess) return false;
+    for (int i = 0; i < moe_handle::NSTAGE; ++i) {
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, e[i], e[i + 1]) != cudaSuccess) return false;
+        h->stage_ms[i] += ms;
+    }
+    --h->ring_pending;
+    return true;
+}
+
+// Records the boundary before stage i (i == NSTAGE: end of the forward).
+inline void mark(moe_handle* h, int i, cudaStream_t st) {
+    if (h->cur) cudaEventRecord(h->cur[i], st);
+}
+
+template <int BN, int STAGES, int EPI>
+cudaError_t launch_tc(const TcParams& prm, int grid, cudaStream_t st) {
+    using S = TcSmem<BN, STAGES>;
+    static bool attr_set[64] = {};  // per instantiation and device, before the first launch
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, EPI>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    tc_gemm_kernel<BN, STAGES, EPI><<<grid, TC_THREADS, S::TOTAL, st>>>(prm);
+    return cudaGetLastError();
+}
+
+// Upper bound of the tiles a launch can have (the exact count depends on
+// the routing, which stays on the device).
+int tile_bound(const TcParams& prm, int BN, int P) {
+    int64_t n = 0;
+    for (int s = 0; s < prm.n_segs; ++s) {
+        const TcSeg& sg = prm.seg[s];
+        const int64_t ntok = sg.grouped ? (static_cast<int64_t>(P) + BN - 1) / BN + prm.E
+                                        : (static_cast<int64_t>(sg.n_rows) + BN - 1) / BN;
+        n += ntok * sg.n_ftiles;
+    }
+    return static_cast<int>(std::min<int64_t>(n, 1 << 30));
+}
+
+template <int EPI>
+cudaError_t run_tc(const TcParams& prm, int BN, int P, int num_sms, cudaStream_t st) {
+    const int grid = std::max(1, std::min(num_sms, tile_bound(prm, BN, P)));
+    if (BN == 256) return launch_tc<256, 4, EPI>(prm, grid, st);
+    return launch_tc<64, 8, EPI>(prm, grid, st);
+}
+
+template <int EPL>
+void launch_topk_e(const float* logits, const float* bias, int T, int E, int k, float scale,
+                   int* idx, float* w, int* chunk_cnt, cudaStream_t st) {
+    const int n_chunks = (T + CHUNK_TOKENS - 1) / CHUNK_TOKENS;
+    topk_kernel<EPL><<<n_chunks, 512, E * sizeof(int), st>>>(logits, bias, T, E, k, scale, idx, w,
+                                                             chunk_cnt);
+}
+
+void launch_topk(const float* logits, const float* bias, int T, int E, int k, float scale,
+                 int* idx, float* w, int* chunk_cnt, cudaStream_t st) {
+    if (E <= 32) launch_topk_e<1>(logits, bias, T, E, k, scale, idx, w, chunk_cnt, st);
+    else if (E <= 64) launch_topk_e<2>(logits, bias, T, E, k, scale, idx, w, chunk_cnt, st);
+    else if (E <= 128) launch_topk_e<4>(logits, bias, T, E, k, scale, idx, w, chunk_cnt, st);
+    else if (E <= 256) launch_topk_e<8>(logits, bias, T, E, k, scale, idx, w, chunk_cnt, st);
+    else if (E <= 512) launch_topk_e<16>(logits, bias, T, E, k, scale, idx, w, chunk_cnt, st);
+    else launch_topk_e<32>(logits, bias, T, E, k, scale, idx, w, chunk_cnt, st);
+}
+
+struct FwdArgs {
+    int T;
+    const void *x, *norm_w, *router_w;
+    const float* bias;
+    const void *gate_up, *down, *sg, *su, *sd;
+    int k;
+    float scale;
+    void* out;
+};
+
+template <typename T>
+moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t st) {
+    const moe_config& c = h->cfg;
+    const int d = c.hidden, E = c.n_experts, I = c.inter, Is = c.shared_inter;
+    const int Tn = a.T, k = a.k, P = Tn * k;
+    const int n_chunks = (Tn + CHUNK_TOKENS - 1) / CHUNK_TOKENS;
+    const T* x = static_cast<const T*>(a.x);
+    T* xn = static_cast<T*>(h->xn);
+
+    // A+B: RMSNorm and router logits
+    mark(h, 0, st);
+    if (h->tc) {
+        rmsnorm_kernel<T><<<Tn, 256, 0, st>>>(x, static_cast<const T*>(a.norm_w), xn, d, c.eps);
+        mark(h, 1, st);
+        TcParams prm;
+        std::memset(&prm, 0, sizeof prm);
+        prm.n_segs = 1;
+        prm.E = E;
+        prm.offsets = h->offsets;
+        prm.err = h->err;
+        if (!map_2d(&prm.a0[0], a.router_w, d, E) || !map_2d(&prm.a1[0], a.router_w, d, E) ||
+            !map_2d(&prm.b[0], xn, d, Tn))
+            return MOE_ERR_CUDA;
+        prm.seg[0] = TcSeg{0, Tn, d, 128, 64, (E + 127) / 128, E, E, h->logits, nullptr};
+        const int BN = (Tn >= 1024) ? 256 : 64;
+        if (run_tc<EPI_LOGITS>(prm, BN, 0, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        h->launches += 2;
+    } else {
+        rmsnorm_router_kernel<T><<<Tn, 256, d * sizeof(float), st>>>(
+            x, static_cast<const T*>(a.norm_w), static_cast<const T*>(a.router_w), xn, h->logits, d,
+            E, c.eps);
+        mark(h, 1, st);
+        h->launches += 1;
+    }
+    // C+D: top-k, weights, chunk histograms; E: scan, scatter, gather
+    mark(h, 2, st);
+    launch_topk(h->logits, a.bias, Tn, E, k, a.scale, h->topk_idx, h->topk_w, h->chunk_cnt, st);
+    mark(h, 3, st);
+    scan_kernel<<<1, std::max(32, (E + 31) / 32 * 32), 0, st>>>(h->chunk_cnt, n_chunks, E,
+                                                               h->counts, h->offsets, h->chunk_base);
+    mark(h, 4, st);
+    scatter_kernel<<<n_chunks, CHUNK_TOKENS, E * (CHUNK_TOKENS / 32) * sizeof(uint32_t), st>>>(
+        h->topk_idx, h->topk_w, Tn, E, k, h->chunk_base, h->pos, h->row_tok, h->row_w);
+    mark(h, 5, st);
+    gather_rows_kernel<T><<<std::min(4 * h->num_sms, (P + 7) / 8), 256, 0, st>>>(
+        xn, h->row_tok, static_cast<T*>(h->xp), P, d, Tn);
+    h->launches += 4;
+    mark(h, 6, st);
+
+    T* hbuf = static_cast<T*>(h->h);
+    T* yp = static_cast<T*>(h->yp);
+    T* hs = static_cast<T*>(h->hs);
+    T* sh = Is > 0 ? static_cast<T*>(h->sh) : nullptr;
+    if (h->tc) {
+        const int BN = (P >= 64 * E) ? 256 : 64;
+        // F+H(gate/up): routed + shared gate|up with SwiGLU epilogue
+        TcParams g1;
+        std::memset(&g1, 0, sizeof g1);
+        g1.E = E;
+        g1.offsets = h->offsets;
+        g1.err = h->err;
+        g1.n_segs = Is > 0 ? 2 : 1;
+        if (!map_3d(&g1.a0[0], a.gate_up, 2 * I, d, E) || !map_3d(&g1.a1[0], a.gate_up, 2 * I, d, E) ||
+            !map_2d(&g1.b[0], h->xp, d, P))
+            return MOE_ERR_CUDA;
+        g1.seg[0] = TcSeg{1, 0, d, 64, I, I / 64, I, I, hbuf, nullptr};
+        if (Is > 0) {
+            if (!map_2d(&g1.a0[1], a.sg, d, Is) || !map_2d(&g1.a1[1], a.su, d, Is) ||
+                !map_2d(&g1.b[1], xn, d, Tn))
+                return MOE_ERR_CUDA;
+            g1.seg[1] = TcSeg{0, Tn, d, 64, 0, Is / 64, Is, Is, hs, nullptr};
+        }
+        if (run_tc<EPI_SWIGLU>(g1, BN, P, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        mark(h, 7, st);
+        // G+H(down): routed down with routing weight + shared down
+        TcParams g2;
+        std::memset(&g2, 0, sizeof g2);
+        g2.E = E;
+        g2.offsets = h->offsets;
+        g2.err = h->err;
+        g2.n_segs = Is > 0 ? 2 : 1;
+        if (!map_3d(&g2.a0[0], a.down, d, I, E) || !map_3d(&g2.a1[0], a.down, d, I, E) ||
+            !map_2d(&g2.b[0], hbuf, I, P))
+            return MOE_ERR_CUDA;
+        g2.seg[0] = TcSeg{1, 0, I, 128, 64, (d + 127) / 128, d, d, yp, h->row_w};
+        if (Is > 0) {
+            if (!map_2d(&g2.a0[1], a.sd, Is, d) || !map_2d(&g2.a1[1], a.sd, Is, d) ||
+                !map_2d(&g2.b[1], hs, Is, Tn))
+                return MOE_ERR_CUDA;
+            g2.seg[1] = TcSeg{0, Tn, Is, 128, 64, (d + 127) / 128, d, d, sh, nullptr};
+        }
+        if (run_tc<EPI_WEIGHTED>(g2, BN, P, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        h->launches += 2;
+    } else {
+        const T* gu = static_cast<const T*>(a.gate_up);
+        const T* dn = static_cast<const T*>(a.down);
+        simt_gate_up_kernel<T><<<dim3(P, (I + 127) / 128), 128, d * sizeof(float), st>>>(
+            static_cast<const T*>(h->xp), gu, h->offsets, E, d, I, hbuf);
+        if (Is > 0)
+            simt_shared_gate_up_kernel<T><<<dim3(Tn, (Is + 127) / 128), 128, d * sizeof(float), st>>>(
+                xn, static_cast<const T*>(a.sg), static_cast<const T*>(a.su), d, Is, hs);
+        mark(h, 7, st);
+        simt_down_kernel<T><<<dim3(P, (d + 127) / 128), 128, I * sizeof(float), st>>>(
+            hbuf, dn, h->offsets, h->row_w, E, I, d, yp);
+        if (Is > 0)
+            simt_shared_down_kernel<T><<<dim3(Tn, (d + 127) / 128), 128, Is * sizeof(float), st>>>(
+                hs, static_cast<const T*>(a.sd), Is, d, sh);
+        h->launches += Is > 0 ? 4 : 2;
+    }
+    // I: combine with the residual
+    mark(h, 8, st);
+    combine_kernel<T><<<Tn, 256, 0, st>>>(x, sh, yp, h->pos, d, k, static_cast<T*>(a.out));
+    h->launches += 1;
+    mark(h, moe_handle::NSTAGE, st);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status validate_forward(moe_handle* h, const FwdArgs& a, bool host_io) {
+    if (!h) return MOE_ERR_INVALID_ARG;
+    const moe_config& c = h->cfg;
+    if (a.T < 0 || a.T > c.max_tokens) return MOE_ERR_INVALID_ARG;
+    if (a.k < 1 || a.k > c.max_top_k || a.k > c.n_experts) return MOE_ERR_INVALID_ARG;
+    if (!std::isfinite(a.scale)) return MOE_ERR_INVALID_ARG;
+    if (a.T == 0) return MOE_OK;  // nothing is read or written
+    if (!a.x || !a.norm_w || !a.router_w || !a.bias || !a.gate_up || !a.down || !a.out)
+        return MOE_ERR_INVALID_ARG;
+    if (c.shared_inter > 0 && (!a.sg || !a.su || !a.sd)) return MOE_ERR_INVALID_ARG;
+    const void* vec_ptrs[] = {a.x, a.norm_w, a.router_w, a.gate_up, a.down, a.out};
+    for (const void* p : vec_ptrs)
+        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (c.shared_inter > 0 && (!aligned16(a.sg) || !aligned16(a.su) || !aligned16(a.sd)))
+        return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(a.bias) & 3u) != 0) return MOE_ERR_INVALID_ARG;
+    if (!host_io) {
+        const size_t es = h->es, d = c.hidden, E = c.n_experts, I = c.inter, Is = c.shared_inter;
+        const size_t out_b = static_cast<size_t>(a.T) * d * es;
+        const struct { const void* p; size_t n; } ins[] = {
+            {a.x, out_b},         {a.norm_w, d * es},        {a.router_w, E * d * es},
+            {a.bias, E * 4},      {a.gate_up, E * d * 2 * I * es}, {a.down, E * I * d * es},
+            {a.sg, Is * d * es},  {a.su, Is * d * es},       {a.sd, d * Is * es}};
+        for (const auto& in : ins)
+            if (overlaps(a.out, out_b, in.p, in.n)) return MOE_ERR_INVALID_ARG;
+    }
+    return MOE_OK;
+}
+
+moe_status forward_impl(moe_handle* h, const FwdArgs& a, cudaStream_t st) {
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+    h->last_T = a.T;
+    h->last_k = a.k;
+    h->forwards += 1;
+    if (a.T == 0) return MOE_OK;
+    h->cur = nullptr;
+    if (h->profiling) {
+        if (h->ring_pending == moe_handle::RING && !fold_oldest(h)) return MOE_ERR_CUDA;
+        h->cur = &h->ev[static_cast<size_t>(h->ring_head) * (moe_handle::NSTAGE + 1)];
+    }
+    moe_status s = h->cfg.dtype == MOE_DTYPE_BF16 ? forward_simt_or_routing<__nv_bfloat16>(h, a, st)
+                                                   : forward_simt_or_routing<float>(h, a, st);
+    if (h->cur) {
+        if (s == MOE_OK) {
+            h->ring_head = (h->ring_head + 1) % moe_handle::RING;
+            h->ring_pending += 1;
+        }
+        h->cur = nullptr;
+    }
+    return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape or configuration";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_OOM: return "out of device memory";
+        case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+moe_status moe_init(const moe_config* cfg, moe_handle** out) {
+    if (!cfg || !out) return MOE_ERR_INVALID_ARG;
+    const moe_config c = *cfg;
+    if (c.max_tokens < 1 || c.hidden < 1 || c.n_experts < 1 || c.n_experts > 1024 ||
+        c.inter < 1 || c.shared_inter < 0 || c.max_top_k < 1 || c.max_top_k > 32 ||
+        c.max_top_k > c.n_experts || (c.dtype != MOE_DTYPE_FP32 && c.dtype != MOE_DTYPE_BF16) ||
+        !(c.eps >= 0.0f) || !std::isfinite(c.eps) || c.device < 0 ||
+        (c.gemm_path != 0 && c.gemm_path != 1))
+        return MOE_ERR_INVALID_ARG;
+    const int es = c.dtype == MOE_DTYPE_BF16 ? 2 : 4;
+    const int vec = 16 / es;  // 16-byte vectors in RMSNorm, gather and combine
+    if (c.hidden % vec != 0 || c.inter % vec != 0 || c.shared_inter % vec != 0)
+        return MOE_ERR_UNSUPPORTED;
+    const bool tc = c.dtype == MOE_DTYPE_BF16 && c.gemm_path == 0;
+    if (tc && (c.hidden % 64 != 0 || c.inter % 64 != 0 || c.shared_inter % 64 != 0))
+        return MOE_ERR_UNSUPPORTED;
+    const int64_t P_max = static_cast<int64_t>(c.max_tokens) * c.max_top_k;
+    if (P_max > (int64_t(1) << 31) - 1) return MOE_ERR_UNSUPPORTED;
+
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || c.device >= ndev) return MOE_ERR_CUDA;
+    if (cudaSetDevice(c.device) != cudaSuccess) return MOE_ERR_CUDA;
+    if (tc && !encoder()) return MOE_ERR_CUDA;
+
+    moe_handle* h = new (std::nothrow) moe_handle();
+    if (!h) return MOE_ERR_OOM;
+    h->cfg = c;
+    h->es = es;
+    h->tc = tc;
+    h->P_max = P_max;
+    h->n_chunks_max = (c.max_tokens + CHUNK_TOKENS - 1) / CHUNK_TOKENS;
+    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, c.device) != cudaSuccess) {
+        delete h;
+        return MOE_ERR_CUDA;
+    }
+    const size_t T = c.max_tokens, d = c.hidden, E = c.n_experts, I = c.inter, Is = c.shared_inter;
+    const size_t P = P_max, k = c.max_top_k, nch = h->n_chunks_max;
+    bool ok = true;
+    auto alloc = [&](auto** p, size_t bytes) {
+        if (!ok) return;
+        void* q = nullptr;
+        if (cudaMalloc(&q, std::max<size_t>(bytes, 256)) != cudaSuccess) ok = false;
+        *p = static_cast<std::remove_reference_t<decltype(*p)>>(q);
+    };
+    alloc(&h->xn, T * d * es);
+    alloc(&h->logits, T * E * 4);
+    alloc(&h->topk_idx, T * k * 4);
+    alloc(&h->topk_w, T * k * 4);
+    alloc(&h->chunk_cnt, nch * E * 4);
+    alloc(&h->chunk_base, nch * E * 4);
+    alloc(&h->counts, E * 4);
+    alloc(&h->offsets, (E + 1) * 4);
+    alloc(&h->pos, T * k * 4);
+    alloc(&h->row_tok, P * 4);
+    alloc(&h->row_w, P * 4);
+    alloc(&h->xp, P * d * es);
+    alloc(&h->h, P * I * es);
+    alloc(&h->yp, P * d * es);
+    alloc(&h->hs, T * std::max<size_t>(Is, 1) * es);
+    alloc(&h->sh, T * d * es);
+    alloc(&h->x_stage, T * d * es);
+    alloc(&h->out_stage, T * d * es);
+    alloc(&h->err, 4);
+    if (ok && cudaMemset(h->err, 0, 4) != cudaSuccess) ok = false;
+    if (!ok) {
+        cudaGetLastError();
+        free_ws(h);
+        delete h;
+        return MOE_ERR_OOM;
+    }
+    *out = h;
+    return MOE_OK;
+}
+
+moe_status moe_forward(moe_handle* h, int32_t T, const void* x, const void* norm_w,
+                       const void* router_w, const float* corr_bias, const void* gate_up,
+                       const void* down, const void* shared_gate, const void* shared_up,
+                       const void* shared_down, int32_t top_k, float routed_scale, void* out,
+                       void* stream) {
+    FwdArgs a{T, x, norm_w, router_w, corr_bias, gate_up, down, shared_gate, shared_up,
+              shared_down, top_k, routed_scale, out};
+    moe_status s = validate_forward(h, a, false);
+    if (s != MOE_OK) return s;
+    return forward_impl(h, a, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_host(moe_handle* h, int32_t T, const void* x_host, const void* norm_w,
+                            const void* router_w, const float* corr_bias, const void* gate_up,
+                            const void* down, const void* shared_gate, const void* shared_up,
+                            const void* shared_down, int32_t top_k, float routed_scale,
+                            void* out_host, void* stream) {
+    FwdArgs a{T, x_host, norm_w, router_w, corr_bias, gate_up, down, shared_gate, shared_up,
+              shared_down, top_k, routed_scale, out_host};
+    moe_status s = validate_forward(h, a, true);
+    if (s != MOE_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+    const size_t bytes = static_cast<size_t>(T) * h->cfg.hidden * h->es;
+    if (bytes && cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    a.x = h->x_stage;
+    a.out = h->out_stage;
+    s = forward_impl(h, a, st);
+    if (s != MOE_OK) return s;
+    if (bytes && cudaMemcpyAsync(out_host, h->out_stage, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return moe_sync_status(h, stream);
+}
+
+moe_status moe_get_routing(moe_handle* h, int32_t* idx, float* w, int32_t* counts, void* stream) {
+    if (!h) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+    const size_t pairs = static_cast<size_t>(h->last_T) * h->last_k;
+    if (idx && pairs &&
+        cudaMemcpyAsync(idx, h->topk_idx, pairs * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (w && pairs &&
+        cudaMemcpyAsync(w, h->topk_w, pairs * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (counts) {
+        cudaError_t e = h->last_T > 0
+                            ? cudaMemcpyAsync(counts, h->counts, h->cfg.n_experts * 4,
+                                              cudaMemcpyDeviceToDevice, st)
+                            : cudaMemsetAsync(counts, 0, h->cfg.n_experts * 4, st);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+moe_status moe_get_intermediate(moe_handle* h, moe_tensor which, void* dst, size_t dst_bytes,
+                                void* stream) {
+    if (!h || !dst) return MOE_ERR_INVALID_ARG;
+    const size_t T = h->last_T, k = h->last_k, d = h->cfg.hidden, E = h->cfg.n_experts;
+    const void* src = nullptr;
+    size_t bytes = 0;
+    switch (which) {
+        case MOE_T_XN: src = h->xn; bytes = T * d * h->es; break;
+        case MOE_T_LOGITS: src = h->logits; bytes = T * E * 4; break;
+        case MOE_T_OFFSETS: src = h->offsets; bytes = (E + 1) * 4; break;
+        case MOE_T_POS: src = h->pos; bytes = T * k * 4; break;
+        case MOE_T_ROW_TOK: src = h->row_tok; bytes = T * k * 4; break;
+        case MOE_T_H: src = h->h; bytes = T * k * h->cfg.inter * h->es; break;
+        case MOE_T_SHARED: src = h->sh; bytes = h->cfg.shared_inter > 0 ? T * d * h->es : 0; break;
+        default: return MOE_ERR_INVALID_ARG;
+    }
+    if (dst_bytes < bytes) return MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+    if (bytes && cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice,
+                                 static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_sync_status(moe_handle* h, void* stream) {
+    if (!h) return MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    int flag = 0;
+    if (cudaMemcpy(&flag, h->err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (flag != 0) {
+        if (cudaMemset(h->err, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_ERR_TIMEOUT;
+    }
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_set_profiling(moe_handle* h, int32_t enable) {
+    if (!h) return MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+    if (enable && h->ev.empty()) {
+        h->ev.resize(static_cast<size_t>(moe_handle::RING) * (moe_handle::NSTAGE + 1));
+        for (auto& e : h->ev)
+            if (cudaEventCreate(&e) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    h->profiling = enable != 0;
+    return MOE_OK;
+}
+
+moe_status moe_read_stats(moe_handle* h, moe_stats* out) {
+    if (!h || !out) return MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+    while (h->ring_pending > 0)
+        if (!fold_oldest(h)) return MOE_ERR_CUDA;
+    std::memset(out, 0, sizeof *out);
+    out->forwards = h->forwards;
+    out->launches = static_cast<int32_t>(h->launches);
+    out->n_stages = moe_handle::NSTAGE;
+    for (int i = 0; i < moe_handle::NSTAGE; ++i) out->stage_ms[i] = static_cast<float>(h->stage_ms[i]);
+    h->forwards = 0;
+    h->launches = 0;
+    for (double& v : h->stage_ms) v = 0.0;
+    return MOE_OK;
+}
+
+moe_status moe_destroy(moe_handle* h) {
+    if (!h) return MOE_OK;
+    cudaSetDevice(h->cfg.device);
+    cudaDeviceSynchronize();
+    for (auto& e : h->ev) cudaEventDestroy(e);
+    free_ws(h);
+    delete h;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,147 @@
+"""Helpers shared by the GPU parity tests, the smoke check and the benchmark:
+run the CUDA path through the C ABI and compare it with the CPU oracle.
+
+Tolerances (floating point):
+  bf16 storage: max|gpu - oracle| <= 2e-2 * rms(oracle) and
+                sum|gpu - oracle| / sum|oracle| <= 5e-3
+  fp32 storage: max|gpu - oracle| <= 1e-4 * rms(oracle)
+Routing: expert ids are compared exactly; a token may differ only when its
+top-k margin b_(k) - b_(k+1) is below 1e-5 (several selections are then
+correct) or when its RMSNorm output differs in some bf16 rounding from the
+oracle's.  Output parity is judged against the oracle run on the GPU's own
+selection, so a correct alternative selection is not counted as an error.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import oracle as orc
+
+NEAR_TIE = 1e-5
+TOL = {"bf16": dict(max_rms=2e-2, mean_rel=5e-3), "fp32": dict(max_rms=1e-4, mean_rel=1e-5)}
+
+
+def to_np_f32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy()
+
+
+def run_gpu(w, dev_inputs, top_k=None, routed_scale=None, gemm_path=0, T=None, keep=True):
+    """Runs one forward through the C ABI; returns numpy copies of the output
+    and of every intermediate the tests inspect."""
+    from mixture_experts_transformer_sigmoid_b300 import binding as B
+    T = dev_inputs["x"].shape[0] if T is None else T
+    k = w.k if top_k is None else top_k
+    scale = w.routed_scale if routed_scale is None else routed_scale
+    layer = B.MoeSublayer(max_tokens=max(T, 1), hidden=w.d, n_experts=w.E, inter=w.I,
+                          shared_inter=w.Is, max_top_k=k, dtype=w.dtype, eps=w.eps,
+                          gemm_path=gemm_path)
+    try:
+        x = dev_inputs["x"][:T]
+        out = layer.forward(x, dev_inputs, k, scale)
+        st = layer.sync_status()
+        assert st == B.MOE_OK, B.status_string(st)
+        res = {"out": to_np_f32(out)}
+        if T > 0:
+            idx, wt, counts = layer.routing()
+            res.update(idx=idx.cpu().numpy(), w=wt.cpu().numpy(), counts=counts.cpu().numpy())
+            if keep:
+                res["xn"] = to_np_f32(layer.intermediate(B.T_XN))
+                res["logits"] = layer.intermediate(B.T_LOGITS).cpu().numpy()
+                res["offsets"] = layer.intermediate(B.T_OFFSETS).cpu().numpy()
+                res["pos"] = layer.intermediate(B.T_POS).cpu().numpy()
+                res["row_tok"] = layer.intermediate(B.T_ROW_TOK).cpu().numpy()
+        assert layer.sync_status() == B.MOE_OK
+        return res
+    finally:
+        layer.close()
+
+
+def check_permutation(g, T, E, k):
+    """Histogram / scan / scatter invariants (bit-exact integer work)."""
+    idx, counts, offsets, pos, row_tok = g["idx"], g["counts"], g["offsets"], g["pos"], g["row_tok"]
+    P = T * k
+    assert idx.shape == (T, k)
+    assert idx.min() >= 0 and idx.max() < E
+    for t in range(min(T, 4096)):
+        assert len(set(idx[t].tolist())) == k, "an expert chosen twice"
+    np.testing.assert_array_equal(counts, np.bincount(idx.ravel(), minlength=E))
+    np.testing.assert_array_equal(offsets, np.concatenate([[0], np.cumsum(counts)]))
+    flat = pos.ravel()
+    assert np.array_equal(np.sort(flat), np.arange(P)), "pos is not a bijection onto the rows"
+    tok = np.repeat(np.arange(T), k)
+    np.testing.assert_array_equal(row_tok[flat], tok)
+    # rows of each expert hold that expert's tokens in ascending order
+    exp_of_row = np.searchsorted(offsets, np.arange(P), side="right") - 1
+    np.testing.assert_array_equal(exp_of_row[flat], idx.ravel())
+    for e in range(E):
+        seg = row_tok[offsets[e]:offsets[e + 1]]
+        assert np.all(np.diff(seg) > 0)
+
+
+def check_xn(g_xn, ref_xn, dtype):
+    if dtype == "fp32":
+        np.testing.assert_allclose(g_xn, ref_xn, rtol=2e-6, atol=1e-6)
+        return 0
+    same = g_xn == ref_xn
+    n_diff = int((~same).sum())
+    assert same.mean() >= 0.999, f"{n_diff} xn elements differ"
+    rel = np.abs(g_xn - ref_xn) / np.maximum(np.abs(ref_xn), 1e-30)
+    assert rel[~same].max(initial=0.0) <= 2.0 ** -7 + 1e-9, "xn differs by more than one bf16 ulp"
+    return n_diff
+
+
+def check_routing_stage(g, host, c, rows=None):
+    """Oracle steps B-D on the GPU's own xn: the expert ids must agree except
+    at near-ties; the logits and weights must agree closely."""
+    sel = slice(None) if rows is None else rows
+    xn = g["xn"][sel]
+    logits, idx, wts, margin = orc.route(c, xn, host["router_w"], host["corr_bias"])
+    gl = g["logits"][sel]
+    scale = max(1.0, float(np.abs(logits).max()))
+    assert np.abs(gl - logits).max() <= 2e-5 * scale, np.abs(gl - logits).max()
+    gi, gw = g["idx"][sel], g["w"][sel]
+    mismatch = np.any(gi != idx, axis=1)
+    bad = mismatch & (margin >= NEAR_TIE)
+    assert not bad.any(), f"{int(bad.sum())} tokens routed differently with margin >= {NEAR_TIE}"
+    ok = ~mismatch
+    np.testing.assert_allclose(gw[ok], wts[ok], rtol=2e-6, atol=1e-7)
+    np.testing.assert_allclose(gw.astype(np.float64).sum(1), c.routed_scale, rtol=2e-6)
+    return int(mismatch.sum())
+
+
+def output_errors(gpu, ref):
+    diff = np.abs(gpu.astype(np.float64) - ref.astype(np.float64))
+    rms = float(np.sqrt(np.mean(ref.astype(np.float64) ** 2)))
+    return {"max_over_rms": float(diff.max() / rms) if rms > 0 else float(diff.max()),
+            "mean_rel": float(diff.sum() / max(np.abs(ref).sum(), 1e-30))}
+
+
+def check_output(g, host, c, dtype, rows=None):
+    """Oracle on the GPU's selection for the given rows; returns error stats
+    of the output and of the MoE delta (out - x)."""
+    rows_arr = np.arange(g["out"].shape[0]) if rows is None else np.asarray(rows)
+    r = orc.forward(c, host, rows=rows_arr, forced_idx=g["idx"][rows_arr])
+    gout = g["out"][rows_arr]
+    st = output_errors(gout, r["out"])
+    x = host["x"][rows_arr]
+    x = (x.astype(np.uint32) << 16).view(np.float32) if x.dtype == np.uint16 else x
+    sd = output_errors(gout - x, r["out"] - x)
+    tol = TOL[dtype]
+    assert st["max_over_rms"] <= tol["max_rms"], st
+    if dtype == "bf16":
+        assert st["mean_rel"] <= tol["mean_rel"], st
+    return {"out": st, "delta": sd}
+
+
+def check_end_to_end_routing(g, host, c, rows):
+    """Oracle's own routing (its own xn) against the GPU's, for the sampled
+    rows: a difference must be a near-tie or follow an xn rounding flip."""
+    r = orc.forward(c, host, rows=np.asarray(rows))
+    gi = g["idx"][rows]
+    mismatch = np.any(gi != r["idx"], axis=1)
+    xn_flip = np.any(g["xn"][rows] != r["xn"], axis=1)
+    unexplained = mismatch & (r["margin"] >= NEAR_TIE) & ~xn_flip
+    assert not unexplained.any(), f"{int(unexplained.sum())} unexplained routing differences"
+    return {"mismatch": int(mismatch.sum()), "near_tie": int((r["margin"] < NEAR_TIE).sum()),
+            "xn_rows_differ": int(xn_flip.sum())}

@@ -1,0 +1,116 @@
+"""The C-ABI library loads and exports what include/moe.h declares, and its
+host-side argument checks reject bad calls before any CUDA work.  Runs
+without a GPU: no call here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from mixture_experts_transformer_sigmoid_b300 import binding as B
+from mixture_experts_transformer_sigmoid_b300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(B.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_config_struct_matches_header():
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct \{(.*?)\} moe_config;", text, re.S).group(1)
+    fields = re.findall(r"(?:int32_t|float)\s+(\w+);", body)
+    assert fields == [f for f, _ in B.MoeConfig._fields_]
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert len(B.status_string(s)) > 0
+    assert B.status_string(0) == "ok"
+    assert B.status_string(99) == "unknown status"
+
+
+def good_cfg(**kw):
+    c = dict(max_tokens=64, hidden=256, n_experts=8, inter=128, shared_inter=128, max_top_k=2,
+             dtype=B.DTYPE_BF16, eps=1e-6, device=0, gemm_path=0)
+    c.update(kw)
+    return B.MoeConfig(**c)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(max_tokens=0), B.MOE_ERR_INVALID_ARG),
+    (dict(hidden=0), B.MOE_ERR_INVALID_ARG),
+    (dict(n_experts=0), B.MOE_ERR_INVALID_ARG),
+    (dict(n_experts=2000), B.MOE_ERR_INVALID_ARG),
+    (dict(max_top_k=0), B.MOE_ERR_INVALID_ARG),
+    (dict(max_top_k=9), B.MOE_ERR_INVALID_ARG),      # > n_experts
+    (dict(dtype=7), B.MOE_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), B.MOE_ERR_INVALID_ARG),
+    (dict(eps=-1.0), B.MOE_ERR_INVALID_ARG),
+    (dict(device=-1), B.MOE_ERR_INVALID_ARG),
+    (dict(gemm_path=5), B.MOE_ERR_INVALID_ARG),
+    (dict(shared_inter=-1), B.MOE_ERR_INVALID_ARG),
+    (dict(hidden=200), B.MOE_ERR_UNSUPPORTED),       # tensor-core path needs multiples of 64
+    (dict(inter=100), B.MOE_ERR_UNSUPPORTED),
+    (dict(hidden=36, dtype=B.DTYPE_FP32), B.MOE_OK),                # valid fp32 shape
+])
+def test_init_rejects_bad_config(lib, kw, status):
+    c = good_cfg(**kw)
+    h = ctypes.c_void_p()
+    rc = lib.moe_init(ctypes.byref(c), ctypes.byref(h))
+    if status == B.MOE_OK:
+        # a valid config: on a machine without a GPU the device query fails
+        if torch.cuda.is_available():
+            assert rc == B.MOE_OK
+            lib.moe_destroy(h)
+        else:
+            assert rc == B.MOE_ERR_CUDA
+        return
+    assert rc == status
+    assert not h.value
+
+
+def test_init_null_arguments(lib):
+    h = ctypes.c_void_p()
+    assert lib.moe_init(None, ctypes.byref(h)) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_init(ctypes.byref(good_cfg()), None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_calls_on_null_handle(lib):
+    p = ctypes.c_void_p(16)
+    assert lib.moe_forward(None, 1, p, p, p, p, p, p, p, p, p, 1, 1.0, p, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_forward_host(None, 1, p, p, p, p, p, p, p, p, p, 1, 1.0, p, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_get_routing(None, None, None, None, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_get_intermediate(None, 0, p, 16, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_sync_status(None, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_destroy(None) == B.MOE_OK
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    B2 = B
+    saved = B2._lib
+    try:
+        B2._lib = None
+        with pytest.raises(RuntimeError):
+            B2.load_library(str(tmp_path / "missing.so"))
+    finally:
+        B2._lib = saved

@@ -1,0 +1,173 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small cases compare every token; the workload-sized cases compare the
+routing of every token (integer work bit-exact, near-ties excepted) and the
+outputs of a seeded sample of tokens.  Tolerances are in tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import parity
+from mixture_experts_transformer_sigmoid_b300 import workloads as wl
+from oracle import oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+W = wl.Workload
+SMALL = {
+    # several tiles in every dimension plus ragged tails
+    "ragged_bf16": W("ragged_bf16", T=300, d=512, E=16, I=192, Is=128, k=4, routed_scale=1.0,
+                     dtype="bf16"),
+    # E not a multiple of the 128-row router tile, d not a multiple of 128
+    "odd_sizes_bf16": W("odd_sizes_bf16", T=257, d=320, E=40, I=128, Is=64, k=3,
+                        routed_scale=2.5, dtype="bf16"),
+    "no_shared_bf16": W("no_shared_bf16", T=130, d=256, E=8, I=64, Is=0, k=2,
+                        routed_scale=1.0, dtype="bf16"),
+    "top1_bf16": W("top1_bf16", T=200, d=256, E=12, I=128, Is=64, k=1, routed_scale=1.0,
+                   dtype="bf16"),
+    "k_equals_E_bf16": W("k_equals_E_bf16", T=70, d=256, E=4, I=64, Is=64, k=4,
+                         routed_scale=1.0, dtype="bf16"),
+    "skewed_bf16": W("skewed_bf16", T=96, d=512, E=32, I=128, Is=128, k=4, routed_scale=2.5,
+                     dtype="bf16", n_hot=4),
+    "many_experts_bf16": W("many_experts_bf16", T=160, d=256, E=300, I=64, Is=64, k=6,
+                           routed_scale=1.0, dtype="bf16"),
+    "one_token_bf16": W("one_token_bf16", T=1, d=512, E=16, I=128, Is=128, k=4,
+                        routed_scale=1.0, dtype="bf16"),
+    # large per-expert groups: several 256-token tiles per expert
+    "big_groups_bf16": W("big_groups_bf16", T=1200, d=256, E=4, I=128, Is=64, k=2,
+                         routed_scale=1.0, dtype="bf16"),
+    "tiny_fp32": wl.WORKLOADS["tiny_fp32"],
+    "ragged_fp32": W("ragged_fp32", T=77, d=128, E=6, I=64, Is=32, k=2, routed_scale=1.0,
+                     dtype="fp32", bias_range=0.1),
+}
+
+
+def device_inputs(inputs):
+    return {k: v.cuda() for k, v in inputs.items()}
+
+
+def full_check(w, gemm_path=0, seed=0):
+    inp = wl.make_inputs(w, seed=seed)
+    host = wl.host_arrays(inp)
+    g = parity.run_gpu(w, device_inputs(inp), gemm_path=gemm_path)
+    c = orc.cfg_from_workload(w)
+    parity.check_permutation(g, w.T, w.E, w.k)
+    r = orc.forward(c, host)
+    parity.check_xn(g["xn"], r["xn"], w.dtype)
+    parity.check_routing_stage(g, host, c)
+    stats = parity.check_output(g, host, c, w.dtype)
+    rt = parity.check_end_to_end_routing(g, host, c, np.arange(w.T))
+    return stats, rt
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_case_matches_oracle(name):
+    stats, rt = full_check(SMALL[name])
+    print(name, stats, rt)
+
+
+def test_cuda_core_expert_path_matches_oracle():
+    """The FFMA expert kernels (the fp32 path) run on bf16 storage too."""
+    stats, _ = full_check(SMALL["ragged_bf16"], gemm_path=1)
+    print(stats)
+
+
+def test_empty_input_queues_nothing():
+    w = SMALL["ragged_bf16"]
+    inp = device_inputs(wl.make_inputs(w))
+    g = parity.run_gpu(w, inp, T=0)
+    assert g["out"].shape == (0, w.d)
+
+
+def test_token_permutation_permutes_outputs():
+    w = SMALL["ragged_bf16"]
+    inp = wl.make_inputs(w)
+    g1 = parity.run_gpu(w, device_inputs(inp))
+    perm = torch.randperm(w.T, generator=torch.Generator().manual_seed(5))
+    inp2 = dict(inp)
+    inp2["x"] = inp["x"][perm].contiguous()
+    g2 = parity.run_gpu(w, device_inputs(inp2))
+    np.testing.assert_array_equal(g2["out"], g1["out"][perm.numpy()])
+    np.testing.assert_array_equal(g2["idx"], g1["idx"][perm.numpy()])
+
+
+def test_deterministic_across_runs():
+    w = SMALL["skewed_bf16"]
+    inp = device_inputs(wl.make_inputs(w))
+    a = parity.run_gpu(w, inp)
+    b = parity.run_gpu(w, inp)
+    np.testing.assert_array_equal(a["out"], b["out"])
+
+
+def test_forward_host_matches_device_forward():
+    from mixture_experts_transformer_sigmoid_b300 import binding as B
+    w = SMALL["ragged_bf16"]
+    inp = device_inputs(wl.make_inputs(w))
+    layer = B.MoeSublayer(max_tokens=w.T, hidden=w.d, n_experts=w.E, inter=w.I,
+                          shared_inter=w.Is, max_top_k=w.k, dtype=w.dtype)
+    try:
+        out_dev = layer.forward(inp["x"], inp, w.k, w.routed_scale)
+        torch.cuda.synchronize()
+        x_h = inp["x"].cpu().pin_memory()
+        out_h = torch.empty_like(x_h).pin_memory()
+        layer.forward_host(x_h, inp, w.k, w.routed_scale, out_h)
+        assert torch.equal(out_h, out_dev.cpu())
+    finally:
+        layer.close()
+
+
+def test_aliasing_output_rejected():
+    from mixture_experts_transformer_sigmoid_b300 import binding as B
+    w = SMALL["ragged_bf16"]
+    inp = device_inputs(wl.make_inputs(w))
+    layer = B.MoeSublayer(max_tokens=w.T, hidden=w.d, n_experts=w.E, inter=w.I,
+                          shared_inter=w.Is, max_top_k=w.k, dtype=w.dtype)
+    try:
+        with pytest.raises(B.MoeError) as e:
+            layer.forward(inp["x"], inp, w.k, w.routed_scale, out=inp["x"])
+        assert e.value.status == B.MOE_ERR_INVALID_ARG
+        with pytest.raises(B.MoeError):
+            layer.forward(inp["x"], inp, w.k + 1, w.routed_scale)       # top_k > max_top_k
+        buf = torch.empty(w.T * w.d + 8, dtype=inp["x"].dtype, device="cuda")
+        x_mis = buf[1:1 + w.T * w.d].view(w.T, w.d)                     # 2-byte offset
+        x_mis.copy_(inp["x"])
+        with pytest.raises(B.MoeError) as e:
+            layer.forward(x_mis, inp, w.k, w.routed_scale)
+        assert e.value.status == B.MOE_ERR_INVALID_ARG
+    finally:
+        layer.close()
+
+
+# ---------------------------------------------------------------- workloads
+SAMPLE = {"small_bf16": 256, "air_prefill": 96, "glm5_prefill": 24, "glm5_decode": 64}
+
+
+def workload_check(name, dev_gen):
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w, device="cuda" if dev_gen else "cpu")
+    dev = device_inputs(inp)
+    g = parity.run_gpu(w, dev)
+    host = wl.host_arrays(inp)
+    del inp
+    c = orc.cfg_from_workload(w)
+    parity.check_permutation(g, w.T, w.E, w.k)
+    n_mis = parity.check_routing_stage(g, host, c)
+    rows = np.sort(np.random.default_rng(0).choice(w.T, size=min(SAMPLE[name], w.T),
+                                                   replace=False))
+    stats = parity.check_output(g, host, c, w.dtype, rows=rows)
+    rt = parity.check_end_to_end_routing(g, host, c, rows)
+    print(name, "stage-mismatch", n_mis, stats, rt)
+
+
+def test_small_bf16_workload():
+    workload_check("small_bf16", dev_gen=False)
+
+
+def test_air_prefill_workload():
+    workload_check("air_prefill", dev_gen=True)
+
+
+@pytest.mark.parametrize("name", ["glm5_decode", "glm5_prefill"])
+def test_glm5_workloads(name):
+    workload_check(name, dev_gen=True)

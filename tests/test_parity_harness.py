@@ -1,0 +1,59 @@
+"""CPU self-test of the parity harness: given the oracle's own results as the
+'device' result, every check passes; given a planted error, the checks fail."""
+import numpy as np
+import pytest
+
+import parity
+from mixture_experts_transformer_sigmoid_b300 import workloads as wl
+from oracle import oracle as orc
+
+
+def fake_gpu(w, host, c):
+    r = orc.forward(c, host)
+    T, k, E = w.T, w.k, w.E
+    idx = r["idx"]
+    counts = np.bincount(idx.ravel(), minlength=E).astype(np.int32)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    order = sorted(range(T * k), key=lambda p: (idx.ravel()[p], p // k))
+    pos = np.empty(T * k, np.int32)
+    pos[np.array(order)] = np.arange(T * k)
+    row_tok = np.empty(T * k, np.int32)
+    row_tok[pos] = np.repeat(np.arange(T), k)
+    return {"out": r["out"], "xn": r["xn"], "logits": r["logits"], "idx": idx, "w": r["w"],
+            "counts": counts, "offsets": offsets, "pos": pos.reshape(T, k), "row_tok": row_tok}
+
+
+@pytest.fixture(scope="module")
+def case():
+    w = wl.Workload("h", T=90, d=128, E=10, I=64, Is=32, k=3, routed_scale=2.5, dtype="bf16")
+    inp = wl.make_inputs(w, seed=3)
+    host = wl.host_arrays(inp)
+    c = orc.cfg_from_workload(w)
+    return w, host, c, fake_gpu(w, host, c)
+
+
+def test_harness_accepts_the_oracle(case):
+    w, host, c, g = case
+    parity.check_permutation(g, w.T, w.E, w.k)
+    parity.check_xn(g["xn"], g["xn"], w.dtype)
+    parity.check_routing_stage(g, host, c)
+    parity.check_output(g, host, c, w.dtype)
+    parity.check_end_to_end_routing(g, host, c, np.arange(w.T))
+
+
+def test_harness_catches_planted_errors(case):
+    w, host, c, g = case
+    bad = dict(g, out=g["out"] * 1.05)
+    with pytest.raises(AssertionError):
+        parity.check_output(bad, host, c, w.dtype)
+    p2 = g["pos"].copy()
+    p2[0, 0], p2[1, 0] = p2[1, 0], p2[0, 0]
+    with pytest.raises(AssertionError):
+        parity.check_permutation(dict(g, pos=p2), w.T, w.E, w.k)
+    i2 = g["idx"].copy()
+    i2[:, [0, 1]] = i2[:, [1, 0]]
+    with pytest.raises(AssertionError):
+        parity.check_routing_stage(dict(g, idx=i2), host, c)
+    w2 = g["w"] * 1.001
+    with pytest.raises(AssertionError):
+        parity.check_routing_stage(dict(g, w=w2), host, c)
