@@ -12,8 +12,8 @@
 //     [offsets[e], offsets[e+1]) of the B matrix; its weights are read
 //     MN-major from the grouped layout ([E, K, F] with F contiguous) through
 //     a 3-D tensor map with the expert index as the outer coordinate.
-//   dense segment: one group of n_rows rows (the shared expert, or the
-//     router); its weights are nn.Linear [F, K] rows, read K-major.
+//   dense segment: one group of n_rows rows (the shared expert); its
+//     weights are nn.Linear [F, K] rows, read K-major.
 // The A tile is two 64-row TMA boxes (rows 0-63 and 64-127 of the MMA's M);
 // for the gate|up launch they are the gate and the up rows of the same 64
 // features, so the SwiGLU can be applied in the epilogue.
@@ -46,7 +46,7 @@ constexpr uint64_t TC_TIMEOUT_NS = 2000000000ull;   // 2 s
 constexpr uint64_t TC_DRAIN_NS = 100000000ull;      // 100 ms
 constexpr int DEVERR_TIMEOUT = 1;
 
-enum EpiKind { EPI_LOGITS = 0, EPI_SWIGLU = 1, EPI_WEIGHTED = 2 };
+enum EpiKind { EPI_SWIGLU = 1, EPI_WEIGHTED = 2 };
 
 struct TcSeg {
     int grouped;          // 1: expert groups from offsets[]; 0: one group of n_rows rows
@@ -57,7 +57,7 @@ struct TcSeg {
     int n_ftiles;         // feature tiles per group
     int F;                // features that exist (stores are guarded by it)
     int ld_out;           // output row stride in elements
-    void* out;            // bf16 (SwiGLU, weighted) or fp32 (logits) output [rows, ld_out]
+    void* out;            // bf16 output [rows, ld_out]
     const float* row_w;   // weighted epilogue: per-row factor; null means 1
 };
 
@@ -359,18 +359,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                             const float wv = sg.row_w ? sg.row_w[row] : 1.0f;
                             out[static_cast<size_t>(row) * sg.ld_out + col] =
                                 __float2bfloat16_rn(__uint_as_float(v[c]) * wv);
-                        }
-                    }
-                } else {
-                    const int col = ti.ftile * sg.a_fstride + q * 32 + lane;
-                    float* out = static_cast<float*>(sg.out);
-                    if (col < sg.F) {
-                        const int cmax = min(32, ti.rows - c0);
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            if (c >= cmax) break;
-                            out[static_cast<size_t>(ti.row0 + c0 + c) * sg.ld_out + col] =
-                                __uint_as_float(v[c]);
                         }
                     }
                 }

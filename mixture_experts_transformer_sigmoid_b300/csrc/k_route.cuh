@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "numeric.cuh"
+
 namespace moe {
 
 constexpr int CHUNK_TOKENS = 128;  // tokens per histogram chunk (topk and scatter agree on it)
@@ -45,13 +47,6 @@ __device__ __forceinline__ void store_vec(T* p, const float (&f)[Elem<T>::V]) {
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
 // --------------------------------------------------------------- RMSNorm
-// Error-free addition (Knuth's two-sum): s + e == a + b exactly.
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-    s = __fadd_rn(a, b);
-    float bp = __fsub_rn(s, a);
-    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
-}
-
 // Block-wide sum of (hi, lo) pairs; every thread receives the total.
 __device__ __forceinline__ void block_sum_pair(float& hi, float& lo, float2* red) {
 #pragma unroll
@@ -59,7 +54,7 @@ __device__ __forceinline__ void block_sum_pair(float& hi, float& lo, float2* red
         float oh = __shfl_xor_sync(0xffffffffu, hi, off);
         float ol = __shfl_xor_sync(0xffffffffu, lo, off);
         float s, e;
-        two_sum(hi, oh, s, e);
+        two_sum_f(hi, oh, s, e);
         hi = s;
         lo = __fadd_rn(__fadd_rn(lo, ol), e);
     }
@@ -75,7 +70,7 @@ __device__ __forceinline__ void block_sum_pair(float& hi, float& lo, float2* red
             float oh = __shfl_xor_sync(0xffffffffu, hi, off);
             float ol = __shfl_xor_sync(0xffffffffu, lo, off);
             float s, e;
-            two_sum(hi, oh, s, e);
+            two_sum_f(hi, oh, s, e);
             hi = s;
             lo = __fadd_rn(__fadd_rn(lo, ol), e);
         }
@@ -103,7 +98,7 @@ __device__ __forceinline__ float row_rrms(const T* xr, int d, float eps, float2*
             float p = __fmul_rn(f[i], f[i]);
             float pe = fmaf(f[i], f[i], -p);  // exact low part of the square
             float s, e;
-            two_sum(hi, p, s, e);
+            two_sum_f(hi, p, s, e);
             hi = s;
             lo = __fadd_rn(lo, __fadd_rn(e, pe));
         }
@@ -136,11 +131,12 @@ __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ ga
 // RMSNorm fused with the router logits on CUDA cores (fp32 accumulation):
 // one block per token; the normalised row stays in shared memory and each
 // warp takes experts e = warp, warp + nwarps, ... with 16-byte loads of the
-// router weight and a warp-shuffle reduction.  Dynamic smem: d floats.
+// router weight and a warp-shuffle reduction.  The logits are written as
+// (value, 0) pairs, the format the top-k kernel reads.  Dynamic smem: d floats.
 template <typename T>
 __global__ void rmsnorm_router_kernel(const T* __restrict__ x, const T* __restrict__ gain,
                                       const T* __restrict__ router_w, T* __restrict__ xn,
-                                      float* __restrict__ logits, int d, int E, float eps) {
+                                      float2* __restrict__ part, int d, int E, float eps) {
     extern __shared__ float xs[];
     __shared__ float2 red[33];
     constexpr int V = Elem<T>::V;
@@ -172,20 +168,23 @@ __global__ void rmsnorm_router_kernel(const T* __restrict__ x, const T* __restri
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) logits[t * E + e] = acc;
+        if (lane == 0) part[t * E + e] = make_float2(acc, 0.f);
     }
 }
 
 // ------------------------------------------------------------------ top-k
-// One warp per token.  s = sigmoid(l), b = s + bias; k rounds of a warp
+// One warp per token.  The logit is the router's (hi, lo) pair rounded once
+// (also written to `logits` for inspection).  s = sigmoid(l), b = s + bias;
+// k rounds of a warp
 // argmax on (b descending, expert index ascending); slot j's expert and
 // sigmoid end up in lane j.  w_j = routed_scale * s_j / sum_i s_i.  Each
 // block covers CHUNK_TOKENS tokens and writes that chunk's expert histogram.
 // EPL = experts per lane (ceil(E / 32)).
 template <int EPL>
-__global__ void topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
-                            int T, int E, int k, float routed_scale, int* __restrict__ idx_out,
-                            float* __restrict__ w_out, int* __restrict__ chunk_cnt) {
+__global__ void topk_kernel(const float2* __restrict__ part, const float* __restrict__ bias,
+                            int T, int E, int k, float routed_scale, float* __restrict__ logits,
+                            int* __restrict__ idx_out, float* __restrict__ w_out,
+                            int* __restrict__ chunk_cnt) {
     extern __shared__ int cnt[];  // [E]
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
@@ -199,7 +198,9 @@ __global__ void topk_kernel(const float* __restrict__ logits, const float* __res
         for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
             if (e < E) {
-                const float l = logits[static_cast<size_t>(t) * E + e];
+                const float2 pv = part[static_cast<size_t>(t) * E + e];
+                const float l = __fadd_rn(pv.x, pv.y);  // the (hi, lo) pair, rounded once
+                logits[static_cast<size_t>(t) * E + e] = l;
                 const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
                 const float b = __fadd_rn(s, bias[e]);
                 sv[i] = s;

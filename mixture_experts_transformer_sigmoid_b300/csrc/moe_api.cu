@@ -2,7 +2,7 @@
 // workspace, TMA tensor-map encoding and the launch sequence of one forward.
 //
 // bf16 forward on one stream (no host synchronisation):
-//   rmsnorm -> router logits (tcgen05 GEMM) -> top-k + chunk histograms ->
+//   rmsnorm -> router logits (tcgen05, split accumulation) -> top-k + chunk histograms ->
 //   scan -> stable scatter -> row gather -> gate|up grouped GEMM with SwiGLU
 //   epilogue (routed experts + shared expert in one launch) -> down grouped
 //   GEMM with routing-weight epilogue (routed + shared in one launch) ->
@@ -24,6 +24,7 @@
 
 #include "k_gemm_tc.cuh"
 #include "k_route.cuh"
+#include "k_router_tc.cuh"
 #include "moe.h"
 
 using namespace moe;
@@ -38,6 +39,7 @@ struct moe_handle {
     // workspace
     void* xn = nullptr;
     float* logits = nullptr;
+    float2* part = nullptr;   // router (hi, lo) partial sums [ksplit][T][E]
     int* topk_idx = nullptr;
     float* topk_w = nullptr;
     int* chunk_cnt = nullptr;
@@ -120,7 +122,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 void free_ws(moe_handle* h) {
-    void* ptrs[] = {h->xn, h->logits, h->topk_idx, h->topk_w, h->chunk_cnt, h->chunk_base,
+    void* ptrs[] = {h->xn, h->logits, h->part, h->topk_idx, h->topk_w, h->chunk_cnt, h->chunk_base,
                     h->counts, h->offsets, h->pos, h->row_tok, h->row_w, h->xp, h->h, h->yp,
                     h->hs, h->sh, h->x_stage, h->out_stage, h->err};
     for (void* p : ptrs)
@@ -185,21 +187,60 @@ cudaError_t run_tc(const TcParams& prm, int BN, int P, int num_sms, cudaStream_t
 }
 
 template <int EPL>
-void launch_topk_e(const float* logits, const float* bias, int T, int E, int k, float scale,
-                   int* idx, float* w, int* chunk_cnt, cudaStream_t st) {
+void launch_topk_e(const float2* part, const float* bias, int T, int E, int k, float scale,
+                   float* logits, int* idx, float* w, int* chunk_cnt, cudaStream_t st) {
     const int n_chunks = (T + CHUNK_TOKENS - 1) / CHUNK_TOKENS;
-    topk_kernel<EPL><<<n_chunks, 512, E * sizeof(int), st>>>(logits, bias, T, E, k, scale, idx, w,
-                                                             chunk_cnt);
+    topk_kernel<EPL><<<n_chunks, 512, E * sizeof(int), st>>>(part, bias, T, E, k, scale, logits,
+                                                             idx, w, chunk_cnt);
 }
 
-void launch_topk(const float* logits, const float* bias, int T, int E, int k, float scale,
-                 int* idx, float* w, int* chunk_cnt, cudaStream_t st) {
-    if (E <= 32) launch_topk_e<1>(logits, bias, T, E, k, scale, idx, w, chunk_cnt, st);
-    else if (E <= 64) launch_topk_e<2>(logits, bias, T, E, k, scale, idx, w, chunk_cnt, st);
-    else if (E <= 128) launch_topk_e<4>(logits, bias, T, E, k, scale, idx, w, chunk_cnt, st);
-    else if (E <= 256) launch_topk_e<8>(logits, bias, T, E, k, scale, idx, w, chunk_cnt, st);
-    else if (E <= 512) launch_topk_e<16>(logits, bias, T, E, k, scale, idx, w, chunk_cnt, st);
-    else launch_topk_e<32>(logits, bias, T, E, k, scale, idx, w, chunk_cnt, st);
+void launch_topk(const float2* part, const float* bias, int T, int E, int k, float scale,
+                 float* logits, int* idx, float* w, int* chunk_cnt, cudaStream_t st) {
+#define MOE_TOPK(EPL) launch_topk_e<EPL>(part, bias, T, E, k, scale, logits, idx, w, chunk_cnt, st)
+    if (E <= 32) MOE_TOPK(1);
+    else if (E <= 64) MOE_TOPK(2);
+    else if (E <= 128) MOE_TOPK(4);
+    else if (E <= 256) MOE_TOPK(8);
+    else if (E <= 512) MOE_TOPK(16);
+    else MOE_TOPK(32);
+#undef MOE_TOPK
+}
+
+// Router logits on the tensor cores.  Split-K is chosen so that small
+// batches still spread over the SMs; the ranges are then added by
+// router_reduce_kernel.  Returns the number of launches (0 on error).
+int launch_router_tc(moe_handle* h, const void* router_w, const void* xn, int T, cudaStream_t st) {
+    const int d = h->cfg.hidden, E = h->cfg.n_experts;
+    RouterParams rp;
+    std::memset(&rp, 0, sizeof rp);
+    if (!map_2d(&rp.a, router_w, d, E) || !map_2d(&rp.b, xn, d, T)) return 0;
+    const int nkb = d / 64;
+    const int tiles0 = ((T + RT_BN - 1) / RT_BN) * ((E + 127) / 128);
+    int ks = std::max(1, std::min((h->num_sms + tiles0 - 1) / tiles0, nkb / 4));
+    const int kbps = (nkb + ks - 1) / ks;
+    ks = (nkb + kbps - 1) / kbps;
+    rp.T = T;
+    rp.E = E;
+    rp.d = d;
+    rp.ksplit = ks;
+    rp.kb_per_split = kbps;
+    rp.part = h->part;
+    rp.err = h->err;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 0;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 RT_SMEM) != cudaSuccess)
+            return 0;
+        attr_set[dev] = true;
+    }
+    router_tc_kernel<<<std::min(h->num_sms, tiles0 * ks), RT_THREADS, RT_SMEM, st>>>(rp);
+    if (ks == 1) return cudaGetLastError() == cudaSuccess ? 1 : 0;
+    const size_t n = static_cast<size_t>(T) * E;
+    router_reduce_kernel<<<static_cast<int>(std::min<size_t>((n + 255) / 256, 4 * h->num_sms)), 256, 0,
+                           st>>>(h->part, ks, n);
+    return cudaGetLastError() == cudaSuccess ? 2 : 0;
 }
 
 struct FwdArgs {
@@ -226,29 +267,20 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     if (h->tc) {
         rmsnorm_kernel<T><<<Tn, 256, 0, st>>>(x, static_cast<const T*>(a.norm_w), xn, d, c.eps);
         mark(h, 1, st);
-        TcParams prm;
-        std::memset(&prm, 0, sizeof prm);
-        prm.n_segs = 1;
-        prm.E = E;
-        prm.offsets = h->offsets;
-        prm.err = h->err;
-        if (!map_2d(&prm.a0[0], a.router_w, d, E) || !map_2d(&prm.a1[0], a.router_w, d, E) ||
-            !map_2d(&prm.b[0], xn, d, Tn))
-            return MOE_ERR_CUDA;
-        prm.seg[0] = TcSeg{0, Tn, d, 128, 64, (E + 127) / 128, E, E, h->logits, nullptr};
-        const int BN = (Tn >= 1024) ? 256 : 64;
-        if (run_tc<EPI_LOGITS>(prm, BN, 0, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
-        h->launches += 2;
+        const int n_router = launch_router_tc(h, a.router_w, xn, Tn, st);
+        if (n_router == 0) return MOE_ERR_CUDA;
+        h->launches += 1 + n_router;
     } else {
         rmsnorm_router_kernel<T><<<Tn, 256, d * sizeof(float), st>>>(
-            x, static_cast<const T*>(a.norm_w), static_cast<const T*>(a.router_w), xn, h->logits, d,
+            x, static_cast<const T*>(a.norm_w), static_cast<const T*>(a.router_w), xn, h->part, d,
             E, c.eps);
         mark(h, 1, st);
         h->launches += 1;
     }
     // C+D: top-k, weights, chunk histograms; E: scan, scatter, gather
     mark(h, 2, st);
-    launch_topk(h->logits, a.bias, Tn, E, k, a.scale, h->topk_idx, h->topk_w, h->chunk_cnt, st);
+    launch_topk(h->part, a.bias, Tn, E, k, a.scale, h->logits, h->topk_idx, h->topk_w, h->chunk_cnt,
+                st);
     mark(h, 3, st);
     scan_kernel<<<1, std::max(32, (E + 31) / 32 * 32), 0, st>>>(h->chunk_cnt, n_chunks, E,
                                                                h->counts, h->offsets, h->chunk_base);
@@ -443,6 +475,8 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out) {
     };
     alloc(&h->xn, T * d * es);
     alloc(&h->logits, T * E * 4);
+    // router partials: the split-K choice keeps ksplit * T below T + 64 * (number of SMs)
+    alloc(&h->part, (T + 64 * static_cast<size_t>(h->num_sms)) * E * sizeof(float2));
     alloc(&h->topk_idx, T * k * 4);
     alloc(&h->topk_w, T * k * 4);
     alloc(&h->chunk_cnt, nch * E * 4);

@@ -84,6 +84,11 @@ WORKLOADS: Dict[str, Workload] = {
                             Is=2048, k=8, routed_scale=2.5, dtype="bf16",
                             n_hot=16,
                             description="T64 d6144 E256 I2048 k8 bf16, 16 hot experts"),
+    # GLM-5 expert shapes with 32 experts and the same tokens per expert as
+    # the prefill workload (2.5 GB of weights): the profiling case.
+    "glm5_slice": Workload("glm5_slice", T=1024, d=6144, E=32, I=2048,
+                           Is=2048, k=8, routed_scale=2.5, dtype="bf16",
+                           description="T1024 d6144 E32 I2048 k8 bf16"),
 }
 
 

@@ -77,18 +77,15 @@ int oracle_rmsnorm(const oracle_cfg* c, int64_t n, const void* x, const void* ga
 
 /* ---- steps B-D: router, selection, weights -------------------------------- */
 
-/* scratch: s [E], b [E], picked [E] (as char) */
-static void route_row(const oracle_cfg* c, const float* xn, const void* Wr, const float* bias,
-                      const int32_t* forced, float* logits, int32_t* idx, float* w,
-                      float* margin, float* s, float* b, char* picked) {
-    const int d = c->d, E = c->E, k = c->k;
+/* Steps C-D for one token from its fp32 logits.
+ * scratch: s [E], b [E], picked [E] (as char) */
+static void select_row(const oracle_cfg* c, const float* logits, const float* bias,
+                       const int32_t* forced, int32_t* idx, float* w, float* margin, float* s,
+                       float* b, char* picked) {
+    const int E = c->E, k = c->k;
     for (int e = 0; e < E; ++e) {
-        double acc = 0.0;
-        for (int j = 0; j < d; ++j) acc += (double)xn[j] * (double)get(Wr, (int64_t)e * d + j, c->dtype);
-        float l = (float)acc;                              /* fp32 router logit */
-        if (logits) logits[e] = l;
-        s[e] = (float)(1.0 / (1.0 + exp(-(double)l)));     /* sigmoid, rounded to fp32 */
-        b[e] = s[e] + bias[e];                             /* biased score, fp32 add */
+        s[e] = (float)(1.0 / (1.0 + exp(-(double)logits[e])));  /* sigmoid, rounded to fp32 */
+        b[e] = s[e] + bias[e];                                    /* biased score, fp32 add */
         picked[e] = 0;
     }
     /* top-k of b: repeatedly take the largest remaining; on equal values the
@@ -121,6 +118,42 @@ static void route_row(const oracle_cfg* c, const float* xn, const void* Wr, cons
         w[j] = (float)((double)c->routed_scale * (double)s[idx[j]] / ssum);
 }
 
+/* Steps B-D for one token.  lbuf [E] receives the logits. */
+static void route_row(const oracle_cfg* c, const float* xn, const void* Wr, const float* bias,
+                      const int32_t* forced, float* lbuf, int32_t* idx, float* w,
+                      float* margin, float* s, float* b, char* picked) {
+    const int d = c->d, E = c->E;
+    for (int e = 0; e < E; ++e) {
+        double acc = 0.0;
+        for (int j = 0; j < d; ++j) acc += (double)xn[j] * (double)get(Wr, (int64_t)e * d + j, c->dtype);
+        lbuf[e] = (float)acc;                              /* fp32 router logit */
+    }
+    select_row(c, lbuf, bias, forced, idx, w, margin, s, b, picked);
+}
+
+int oracle_select(const oracle_cfg* c, int64_t n, const float* logits, const float* corr_bias,
+                  int32_t* idx, float* w, float* margin) {
+    if (!c || !logits || !corr_bias || !idx || !w || n < 0 || c->k < 1 || c->k > c->E) return 1;
+    int failed = 0;
+#pragma omp parallel
+    {
+        float* s = (float*)malloc(sizeof(float) * c->E);
+        float* b = (float*)malloc(sizeof(float) * c->E);
+        char* picked = (char*)malloc(c->E);
+        if (!s || !b || !picked) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int64_t t = 0; t < n; ++t)
+                select_row(c, logits + t * c->E, corr_bias, NULL, idx + t * c->k, w + t * c->k,
+                           margin ? margin + t : NULL, s, b, picked);
+        }
+        free(s); free(b); free(picked);
+    }
+    return failed ? 2 : 0;
+}
+
 int oracle_route(const oracle_cfg* c, int64_t n, const float* xn, const void* router_w,
                  const float* corr_bias, float* logits, int32_t* idx, float* w, float* margin) {
     if (!c || !xn || !router_w || !corr_bias || n < 0 || c->k < 1 || c->k > c->E) return 1;
@@ -129,25 +162,27 @@ int oracle_route(const oracle_cfg* c, int64_t n, const float* xn, const void* ro
     {
         float* s = (float*)malloc(sizeof(float) * c->E);
         float* b = (float*)malloc(sizeof(float) * c->E);
+        float* lb = (float*)malloc(sizeof(float) * c->E);
         char* picked = (char*)malloc(c->E);
         int32_t* idx_t = (int32_t*)malloc(sizeof(int32_t) * c->k);
         float* w_t = (float*)malloc(sizeof(float) * c->k);
-        if (!s || !b || !picked || !idx_t || !w_t) {
+        if (!s || !b || !lb || !picked || !idx_t || !w_t) {
 #pragma omp atomic write
             failed = 1;
         } else {
 #pragma omp for schedule(static)
             for (int64_t t = 0; t < n; ++t) {
-                route_row(c, xn + t * c->d, router_w, corr_bias, NULL,
-                          logits ? logits + t * c->E : NULL, idx_t, w_t,
+                route_row(c, xn + t * c->d, router_w, corr_bias, NULL, lb, idx_t, w_t,
                           margin ? margin + t : NULL, s, b, picked);
+                for (int e = 0; e < c->E; ++e)
+                    if (logits) logits[t * c->E + e] = lb[e];
                 for (int j = 0; j < c->k; ++j) {
                     if (idx) idx[t * c->k + j] = idx_t[j];
                     if (w) w[t * c->k + j] = w_t[j];
                 }
             }
         }
-        free(s); free(b); free(picked); free(idx_t); free(w_t);
+        free(s); free(b); free(lb); free(picked); free(idx_t); free(w_t);
     }
     return failed ? 2 : 0;
 }
@@ -216,13 +251,14 @@ int oracle_forward(const oracle_cfg* c, int64_t n, const int64_t* rows,
         float* xn = (float*)malloc(sizeof(float) * d);
         float* s = (float*)malloc(sizeof(float) * E);
         float* b = (float*)malloc(sizeof(float) * E);
+        float* lb = (float*)malloc(sizeof(float) * E);
         char* picked = (char*)malloc(E);
         int32_t* sel = (int32_t*)malloc(sizeof(int32_t) * k);
         float* wt = (float*)malloc(sizeof(float) * k);
         double* acc = (double*)malloc(sizeof(double) * d);
         double* g = (double*)malloc(sizeof(double) * hmax);
         double* u = (double*)malloc(sizeof(double) * I);
-        if (!xn || !s || !b || !picked || !sel || !wt || !acc || !g || !u) {
+        if (!xn || !s || !b || !lb || !picked || !sel || !wt || !acc || !g || !u) {
 #pragma omp atomic write
             failed = 1;
         } else {
@@ -230,9 +266,9 @@ int oracle_forward(const oracle_cfg* c, int64_t n, const int64_t* rows,
             for (int64_t t = 0; t < n; ++t) {
                 int64_t row = rows ? rows[t] : t;
                 rmsnorm_row(c, x, row, gain, xn);
-                route_row(c, xn, router_w, corr_bias, forced_idx ? forced_idx + t * k : NULL,
-                          logits ? logits + t * E : NULL, sel, wt,
-                          margin ? margin + t : NULL, s, b, picked);
+                route_row(c, xn, router_w, corr_bias, forced_idx ? forced_idx + t * k : NULL, lb,
+                          sel, wt, margin ? margin + t : NULL, s, b, picked);
+                if (logits) memcpy(logits + t * E, lb, sizeof(float) * E);
                 for (int o = 0; o < d; ++o) acc[o] = 0.0;
                 if (c->Is > 0) shared_expert(c, xn, shared_gate, shared_up, shared_down, acc, g);
                 for (int j = 0; j < k; ++j) {
@@ -249,7 +285,7 @@ int oracle_forward(const oracle_cfg* c, int64_t n, const int64_t* rows,
                 if (xn_out) memcpy(xn_out + t * d, xn, sizeof(float) * d);
             }
         }
-        free(xn); free(s); free(b); free(picked); free(sel); free(wt); free(acc); free(g); free(u);
+        free(xn); free(s); free(b); free(lb); free(picked); free(sel); free(wt); free(acc); free(g); free(u);
     }
     return failed ? 2 : 0;
 }

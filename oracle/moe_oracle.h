@@ -61,6 +61,10 @@ int oracle_rmsnorm(const oracle_cfg* c, int64_t n, const void* x, const void* ga
 int oracle_route(const oracle_cfg* c, int64_t n, const float* xn, const void* router_w,
                  const float* corr_bias, float* logits, int32_t* idx, float* w, float* margin);
 
+/* Steps C-D given fp32 logits [n, E]: idx [n, k], w [n, k], margin [n] (may be NULL). */
+int oracle_select(const oracle_cfg* c, int64_t n, const float* logits, const float* corr_bias,
+                  int32_t* idx, float* w, float* margin);
+
 /* The whole sublayer for the rows listed in `rows` (n of them; NULL = rows
  * 0..n-1 of x).  out [n, d] fp32.  Optional outputs may be NULL: idx [n,k],
  * w [n,k], margin [n], xn [n,d], logits [n,E].  When forced_idx [n,k] is not

@@ -52,13 +52,14 @@ def load():
         lib.oracle_rmsnorm.argtypes = [ctypes.POINTER(OracleCfg), ctypes.c_int64, P, P, P]
         lib.oracle_route.argtypes = [ctypes.POINTER(OracleCfg), ctypes.c_int64, P, P, P,
                                      P, P, P, P]
+        lib.oracle_select.argtypes = [ctypes.POINTER(OracleCfg), ctypes.c_int64, P, P, P, P, P]
         lib.oracle_forward.argtypes = [ctypes.POINTER(OracleCfg), ctypes.c_int64, P,
                                        P, P, P, P, P, P, P, P, P, P,
                                        P, P, P, P, P, P]
         lib.oracle_param_count.argtypes = [ctypes.POINTER(OracleCfg)]
         lib.oracle_param_count.restype = ctypes.c_int64
         lib.oracle_num_threads.restype = ctypes.c_int
-        for f in (lib.oracle_rmsnorm, lib.oracle_route, lib.oracle_forward):
+        for f in (lib.oracle_rmsnorm, lib.oracle_route, lib.oracle_select, lib.oracle_forward):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -107,6 +108,20 @@ def route(c: OracleCfg, xn: np.ndarray, router_w: np.ndarray, bias: np.ndarray):
                              _ptr(logits), _ptr(idx), _ptr(w), _ptr(margin))
     assert rc == 0, rc
     return logits, idx, w, margin
+
+
+def select(c: OracleCfg, logits: np.ndarray, bias: np.ndarray):
+    """Steps C-D on given fp32 logits [n, E].  Returns idx, w, margin."""
+    logits = np.ascontiguousarray(logits, np.float32)
+    bias = np.ascontiguousarray(bias, np.float32)
+    n = logits.shape[0]
+    idx = np.empty((n, c.k), np.int32)
+    w = np.empty((n, c.k), np.float32)
+    margin = np.empty((n,), np.float32)
+    rc = load().oracle_select(ctypes.byref(c), n, _ptr(logits), _ptr(bias), _ptr(idx), _ptr(w),
+                              _ptr(margin))
+    assert rc == 0, rc
+    return idx, w, margin
 
 
 def forward(c: OracleCfg, a: dict, rows: Optional[np.ndarray] = None,

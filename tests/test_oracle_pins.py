@@ -372,3 +372,33 @@ def test_forced_selection():
     _, s, _ = numpy_scores(r["xn"], a["router_w"], a["corr_bias"])
     sel = np.take_along_axis(s, other, 1).astype(np.float64)
     np.testing.assert_allclose(f["w"], sel / sel.sum(1, keepdims=True), rtol=2e-7)
+
+
+@pytest.mark.parametrize("E,k", [(5, 2), (9, 3)])
+def test_select_from_logits_matches_bruteforce(E, k):
+    """Steps C-D alone, on given logits: the brute-force k-subset with the
+    largest biased sum, slot order by biased score, weights from the
+    unbiased sigmoids."""
+    rng = np.random.default_rng(200 + E)
+    T = 150
+    c = orc.cfg(32, E, 16, 0, k, "fp32", routed_scale=2.5)
+    logits = (rng.standard_normal((T, E)) * 2).astype(np.float32)
+    bias = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+    idx, w, margin = orc.select(c, logits, bias)
+    s = (1.0 / (1.0 + np.exp(-logits.astype(np.float64)))).astype(np.float32)
+    b = (s + bias).astype(np.float32)
+    for t in range(T):
+        best = max(itertools.combinations(range(E), k),
+                   key=lambda sub: (math.fsum(sorted(float(b[t, e]) for e in sub)),
+                                    [-e for e in sub]))
+        assert idx[t].tolist() == sorted(best, key=lambda e: (-float(b[t, e]), e))
+        sel = s[t, idx[t]].astype(np.float64)
+        np.testing.assert_allclose(w[t], 2.5 * sel / sel.sum(), rtol=2e-7)
+    # route() = step B followed by select() on its own logits
+    xn = rng.standard_normal((T, 32)).astype(np.float32)
+    Wr = (rng.standard_normal((E, 32)) * 0.3).astype(np.float32)
+    lg, idx2, w2, m2 = orc.route(c, xn, Wr, bias)
+    idx3, w3, m3 = orc.select(c, lg, bias)
+    np.testing.assert_array_equal(idx2, idx3)
+    np.testing.assert_array_equal(w2, w3)
+    np.testing.assert_array_equal(m2, m3)
