@@ -1,0 +1,405 @@
+#!/usr/bin/env python3
+"""Throughput of the GLM MoE feed-forward sublayer forward pass on B300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload glm5_prefill] [--no-decode] [--no-cpu-baseline]
+
+One step is one forward pass of the whole sublayer (RMSNorm, sigmoid router
+and top-k, permutation, routed SwiGLU experts, shared expert, combine and
+residual) over one batch of synthetic tokens already resident in HBM.  With
+N > 1 (launched by torch.distributed.run) every rank holds a full replica of
+the weights and runs its own batch: no collective is on the data path, so
+scaling is weak and the value is the tokens of all ranks per second.
+
+Rank 0 prints one JSON line.  ``--impl reference`` times the CPU oracle (the
+plain definition of the sublayer, run on the host cores) on a bounded sample
+of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_transformer_sigmoid_b300 import workloads as wl  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+METRIC = "MoE sublayer tokens/s"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return json.load(open(p)), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------ arithmetic
+def gate_up_flops(w, T):
+    return 4.0 * T * w.k * w.d * w.I + 4.0 * T * w.d * w.Is
+
+
+def down_flops(w, T):
+    return 2.0 * T * w.k * w.I * w.d + 2.0 * T * w.Is * w.d
+
+
+def total_flops(w, T):
+    return 2.0 * T * w.d * w.E + gate_up_flops(w, T) + down_flops(w, T)
+
+
+def weight_bytes(w):
+    es = 4 if w.dtype == "fp32" else 2
+    return es * (w.E * w.d * 3 * w.I + 3 * w.d * w.Is + w.E * w.d + w.d) + 4 * w.E
+
+
+def decode_bytes(w, T, n_active):
+    """Bytes a decode forward must move: the weights of every expert that
+    received a token, the shared expert, the router, x in and out."""
+    return (n_active + 1) * 3 * w.d * w.I * 2 + w.E * w.d * 2 + w.E * 4 + 2 * T * w.d * 2
+
+
+def gate_up_decode_bytes(w, n_active):
+    return n_active * w.d * 2 * w.I * 2 + 2 * w.d * w.Is * 2
+
+
+# ------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.samples = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", gpu_index, "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                self.samples.append({"sm": float(f[1]), "max": float(f[2]), "power": float(f[3]),
+                                     "hw": f[5], "hw_thermal": f[6], "sw_thermal": f[7],
+                                     "sw_power": f[8]})
+            except ValueError:
+                continue
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        pw = [s["power"] for s in self.samples]
+        thr = min(pw) + 0.5 * (max(pw) - min(pw)) if max(pw) - min(pw) > 50 else -1.0
+        load = [s for s in self.samples if s["power"] >= thr] or self.samples
+        reasons = set()
+        for s in load:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if s[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s["sm"] for s in load),
+                "sm_max_mhz": max(s["max"] for s in load), "reasons": sorted(reasons),
+                "samples": len(load), "power_w_median": statistics.median(s["power"] for s in load)}
+
+
+# ------------------------------------------------------------ helpers
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def gpu_index(local):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(ids):
+            return ids[local]
+    return str(local)
+
+
+def oracle_sample(w, host, n_tokens, seed=1):
+    """Runs the CPU oracle on n_tokens seeded tokens; returns (seconds, tokens)."""
+    from oracle import oracle as orc
+    c = orc.cfg_from_workload(w)
+    rows = np.sort(np.random.default_rng(seed).choice(w.T, size=min(n_tokens, w.T), replace=False))
+    t0 = time.perf_counter()
+    orc.forward(c, host, rows=rows)
+    return time.perf_counter() - t0, len(rows)
+
+
+def cpu_baseline(w, host, target_s=15.0):
+    """The oracle timed on the host cores on a bounded sample (about
+    target_s seconds of CPU work), as tokens/s."""
+    from oracle import oracle as orc
+    t, _ = oracle_sample(w, host, 8, seed=2)            # calibration
+    n2 = int(min(w.T, max(8, round(8 * target_s / max(t, 1e-3)))))
+    t2, n2 = oracle_sample(w, host, n2, seed=3)
+    return {"value": round(n2 / t2, 3), "unit": "tokens/s", "cores": orc.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n2} seeded tokens of the {w.name} workload ({t2:.1f} s, fp64 oracle)"}
+
+
+# ------------------------------------------------------------ our arm
+def run_ours(args, world, rank, local):
+    from mixture_experts_transformer_sigmoid_b300 import binding as B
+    peaks, peak_src = load_peaks()
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w, seed=0, device="cuda")
+    if rank > 0:   # each replica its own batch, the same weights
+        inp["x"] = wl.make_inputs(w, seed=rank, device="cuda", weights_from=inp)["x"]
+    torch.cuda.synchronize()
+    T = w.T
+    layer = B.MoeSublayer(max_tokens=T, hidden=w.d, n_experts=w.E, inter=w.I, shared_inter=w.Is,
+                          max_top_k=w.k, dtype=w.dtype, eps=w.eps, device=local)
+    out = torch.empty_like(inp["x"])
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(gpu_index(local))
+    time.sleep(0.3)
+
+    for _ in range(args.warmup):
+        layer.forward(inp["x"], inp, w.k, w.routed_scale, out=out)
+    assert layer.sync_status() == B.MOE_OK
+    layer.set_profiling(True)
+    layer.read_stats()
+
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        layer.forward(inp["x"], inp, w.k, w.routed_scale, out=out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1) / args.steps
+    st = layer.read_stats()
+    layer.set_profiling(False)
+    assert layer.sync_status() == B.MOE_OK
+    ms_max = max_over_ranks(ms, world)
+    value = world * T / (ms_max / 1e3)
+
+    stage_ms = {k: v / args.steps for k, v in st["stage_ms"].items()}
+    gu_ms, dn_ms = stage_ms["gate_up_swiglu"], stage_ms["down_weighted"]
+    dominant = "gate_up_swiglu" if gu_ms >= dn_ms else "down_weighted"
+    dom_ms = gu_ms if dominant == "gate_up_swiglu" else dn_ms
+    dom_flops = gate_up_flops(w, T) if dominant == "gate_up_swiglu" else down_flops(w, T)
+    dom_tf = dom_flops / (dom_ms / 1e3) / 1e12
+    peak_tf = peaks["bf16_tflops"]
+    roofline = {"kernel": f"tc_gemm_kernel ({dominant})", "bound": "tensor",
+                "achieved": round(dom_tf, 1), "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": round(dom_tf / peak_tf, 4),
+                "frac_of_sustained": round(dom_tf / peaks["bf16_tflops_sustained"], 4),
+                "peak_source": f"{peak_src} bf16 dense (burst)",
+                "flops_per_launch": dom_flops, "avg_launch_ms": round(dom_ms, 4),
+                "traffic": None}
+    whole_tf = total_flops(w, T) / (ms / 1e3) / 1e12
+    l2 = (f"inputs larger than L2 ({weight_bytes(w) / 1e9:.1f} GB of weights read every step)"
+          if weight_bytes(w) > 126e6 else "inputs smaller than L2")
+    res = {
+        "metric": f"{METRIC} ({w.name})", "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": w.name, "tokens_per_gpu": T, "global_tokens": world * T,
+                   "hidden": w.d, "experts": w.E, "inter": w.I, "shared_inter": w.Is,
+                   "top_k": w.k, "routed_scale": w.routed_scale,
+                   "parallelism": f"replicas x{world} (no collective)", "l2": l2},
+        "tflops_whole_step": round(whole_tf, 1),
+        "tensor_frac_whole_step": round(whole_tf / peak_tf, 4),
+        "roofline": roofline,
+        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "gpu_launches": st["launches"],
+    }
+
+    # ---- decode: GLM-5 shapes, T = 64, skewed routing, L2 flushed per step
+    if args.decode and w.name == "glm5_prefill":
+        res["decode"] = run_decode(args, inp, local, peaks, peak_src, world)
+
+    # ---- end to end: host buffers through moe_forward_host
+    x_h = inp["x"].cpu().pin_memory()
+    out_h = torch.empty_like(x_h).pin_memory()
+    for _ in range(2):
+        layer.forward_host(x_h, inp, w.k, w.routed_scale, out_h)
+    ke = max(3, min(args.steps, 20))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(ke):
+        layer.forward_host(x_h, inp, w.k, w.routed_scale, out_h)
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / ke, world)
+    res["e2e"] = {"value": round(world * T / e2e_s, 1), "unit": "tokens/s",
+                  "h2d_bytes_per_step": x_h.numel() * x_h.element_size(),
+                  "d2h_bytes_per_step": out_h.numel() * out_h.element_size(),
+                  "ms_per_step": round(e2e_s * 1e3, 3)}
+    sampler.stop()
+    res["clocks"] = sampler.summary()
+
+    # ---- CPU baseline: the oracle on the host cores, rank 0 at N = 1 only
+    if args.cpu_baseline and world == 1 and rank == 0:
+        host = wl.host_arrays(inp)
+        res["cpu_baseline"] = cpu_baseline(w, host)
+    layer.close()
+    return res
+
+
+def run_decode(args, inp3, local, peaks, peak_src, world):
+    from mixture_experts_transformer_sigmoid_b300 import binding as B
+    w = wl.WORKLOADS["glm5_decode"]
+    dinp = wl.make_inputs(w, seed=0, device="cuda", weights_from=inp3)
+    layer = B.MoeSublayer(max_tokens=w.T, hidden=w.d, n_experts=w.E, inter=w.I,
+                          shared_inter=w.Is, max_top_k=w.k, dtype=w.dtype, eps=w.eps, device=local)
+    out = torch.empty_like(dinp["x"])
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(5):
+        layer.forward(dinp["x"], dinp, w.k, w.routed_scale, out=out)
+    assert layer.sync_status() == B.MOE_OK
+    _, _, counts = layer.routing()
+    n_active = int((counts > 0).sum().item())
+    layer.set_profiling(True)
+    layer.read_stats()
+    n_iter = max(50, args.steps * 4)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_iter)]
+    for a, b in evs:
+        flush.zero_()                       # evict the previous step's weights from L2
+        a.record(stream)
+        layer.forward(dinp["x"], dinp, w.k, w.routed_scale, out=out)
+        b.record(stream)
+    torch.cuda.synchronize()
+    times = [a.elapsed_time(b) for a, b in evs]
+    st = layer.read_stats()
+    layer.set_profiling(False)
+    layer.close()
+    ms = statistics.median(times)
+    nbytes = decode_bytes(w, w.T, n_active)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    stage_ms = {k: v / n_iter for k, v in st["stage_ms"].items()}
+    gu_ms = stage_ms["gate_up_swiglu"]
+    gu_bytes = gate_up_decode_bytes(w, n_active)
+    gu_gbs = gu_bytes / (gu_ms / 1e3) / 1e9
+    hbm = peaks["hbm_gbs"]
+    return {"workload": w.name, "tokens": w.T, "n_active_experts": n_active,
+            "ms_per_step_median": round(ms, 4), "ms_per_step_mean": round(statistics.mean(times), 4),
+            "tokens_per_s": round(world * w.T / (ms / 1e3), 1),
+            "bytes_per_step": nbytes, "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
+            "l2": "256 MB buffer written between steps (outside the timed events)",
+            "roofline": {"kernel": "tc_gemm_kernel (gate_up_swiglu)", "bound": "hbm",
+                         "achieved": round(gu_gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gu_gbs / hbm, 4), "peak_source": f"{peak_src} HBM copy",
+                         "bytes_per_launch": gu_bytes, "avg_launch_ms": round(gu_ms, 4),
+                         "traffic": None},
+            "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}}
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args, world):
+    """The CPU oracle on the host cores, on bounded samples of the workload."""
+    from oracle import oracle as orc
+    w = wl.WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = wl.make_inputs(w, seed=0, device=dev)
+    host = wl.host_arrays(inp)
+    del inp
+    t_cal, n_cal = oracle_sample(w, host, 4, seed=10)
+    per_tok = t_cal / n_cal
+    n_step = int(max(1, min(w.T, args.ref_budget_s / (args.steps + args.warmup) / per_tok)))
+    for i in range(args.warmup):
+        oracle_sample(w, host, n_step, seed=100 + i)
+    times = [oracle_sample(w, host, n_step, seed=1000 + i)[0] for i in range(args.steps)]
+    total_t = sum(times)
+    value = args.steps * n_step / total_t
+    sample = (f"{n_step} seeded tokens of the {w.name} workload per step "
+              f"(T={w.T} in the full workload), fp64 oracle")
+    return {"impl": "reference", "metric": f"{METRIC} ({w.name})", "value": round(value, 3),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * total_t / args.steps, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, random-init weights)",
+            "config": {"workload": w.name, "tokens_per_step": n_step, "hidden": w.d,
+                       "experts": w.E, "inter": w.I, "shared_inter": w.Is, "top_k": w.k,
+                       "routed_scale": w.routed_scale},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s",
+                             "cores": orc.num_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="glm5_prefill", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--no-decode", dest="decode", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--ref-budget-s", type=float, default=150.0,
+                    help="reference arm: seconds of oracle work for the whole run")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, world)), flush=True)
+        return
+    world, rank, local = dist_setup()
+    res = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
