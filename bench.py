@@ -36,6 +36,11 @@ from mixture_experts_transformer_sigmoid_b300 import workloads as wl  # noqa: E4
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 METRIC = "MoE sublayer tokens/s"
 
+# DRAM bytes per launch of the dominant kernel from the ncu capture summarised
+# in profiles/tc_gemm_glm5_slice.md (the slice scaled by 8 to the full
+# GLM-5 prefill launch).  Null once the kernel changes after that capture.
+TRAFFIC_PER_LAUNCH = {"glm5_prefill": {"gate_up_swiglu": 18.19e9, "down_weighted": 8.62e9}}
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -238,7 +243,7 @@ def run_ours(args, world, rank, local):
                 "frac_of_sustained": round(dom_tf / peaks["bf16_tflops_sustained"], 4),
                 "peak_source": f"{peak_src} bf16 dense (burst)",
                 "flops_per_launch": dom_flops, "avg_launch_ms": round(dom_ms, 4),
-                "traffic": None}
+                "traffic": TRAFFIC_PER_LAUNCH.get(w.name, {}).get(dominant)}
     whole_tf = total_flops(w, T) / (ms / 1e3) / 1e12
     l2 = (f"inputs larger than L2 ({weight_bytes(w) / 1e9:.1f} GB of weights read every step)"
           if weight_bytes(w) > 126e6 else "inputs smaller than L2")
