@@ -173,6 +173,40 @@ MOE_API moe_status moe_read_stats(moe_handle* h, moe_stats* out);
 /* Frees the workspace (synchronises the device first).  NULL is a no-op. */
 MOE_API moe_status moe_destroy(moe_handle* h);
 
+/* Routing of a batch from given router logits, with no allocation of any
+ * kind.  It has no counterpart in the paper.  It is there for callers that
+ * cannot call cudaMalloc: a serving engine that reserved all device memory
+ * for its own pool up front, or code that must not let a cudaMalloc or
+ * cudaFree synchronise the device in the middle of its work.
+ *
+ * It runs the routing part of moe_forward on the calling thread's current
+ * device: s = sigmoid(logits), top_k experts by s + corr_bias (ties to the lower
+ * index), w = routed_scale * s / sum(s), the expert histogram, its
+ * exclusive scan and the stable scatter.  Given the logits moe_forward
+ * used (MOE_T_LOGITS), every output equals moe_forward's bit for bit.
+ * All pointers are device memory of the current device, 4-byte aligned,
+ * owned by the caller:
+ *   logits  [T, E] fp32 in;  corr_bias [E] fp32 in
+ *   idx [T, top_k] int32, w [T, top_k] fp32      experts and weights, slot order
+ *   counts [E] int32, offsets [E + 1] int32      tokens per expert, first row of each
+ *   pos [T, top_k] int32                         permuted row of each (token, slot)
+ *   row_tok [T * top_k] int32, row_w [T * top_k] fp32   token and weight of each row
+ * Its scratch (per-chunk histograms) is a 1 MB static device array that
+ * every GPU loading the library holds until the process exits; the limit
+ * is ceil(T / 128) * E <= 131072 (e.g. T = 65536 with E = 256), beyond
+ * which it returns MOE_ERR_UNSUPPORTED before queueing anything.  Every
+ * call on a device shares that array, which keeps the last call's
+ * contents: calls that overlap on the GPU (other streams, other threads)
+ * race, so serialise them.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call
+ * before any stream capture.  1 <= E <= 1024, 1 <= top_k <= min(E, 32),
+ * T >= 0 (T == 0 queues nothing); MOE_ERR_INVALID_ARG for other values or
+ * null/misaligned pointers.  Asynchronous on `stream`. */
+MOE_API moe_status moe_route_static(int32_t T, int32_t E, int32_t top_k, float routed_scale,
+                            const float* logits, const float* corr_bias, int32_t* idx, float* w,
+                            int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* row_tok,
+                            float* row_w, void* stream);
+
 /* Static description of a status code. */
 MOE_API const char* moe_status_string(moe_status s);
 

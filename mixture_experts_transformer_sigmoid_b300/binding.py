@@ -23,7 +23,7 @@ T_XN, T_LOGITS, T_OFFSETS, T_POS, T_ROW_TOK, T_H, T_SHARED = range(7)
 # Functions the header declares (kept in sync by the ABI test).
 EXPORTS = ("moe_init", "moe_forward", "moe_forward_host", "moe_get_routing",
            "moe_get_intermediate", "moe_sync_status", "moe_set_profiling", "moe_read_stats",
-           "moe_destroy", "moe_status_string")
+           "moe_destroy", "moe_route_static", "moe_status_string")
 STAGES = ("rmsnorm", "router", "topk", "scan", "scatter", "gather", "gate_up_swiglu",
           "down_weighted", "combine")
 
@@ -70,6 +70,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_set_profiling.argtypes = [P, I32]
     lib.moe_read_stats.argtypes = [P, ctypes.POINTER(MoeStats)]
     lib.moe_destroy.argtypes = [P]
+    lib.moe_route_static.argtypes = [I32, I32, I32, F32, P, P, P, P, P, P, P, P, P, P]
     lib.moe_status_string.argtypes = [ctypes.c_int]
     lib.moe_status_string.restype = ctypes.c_char_p
     for name in EXPORTS[:-1]:
@@ -187,3 +188,38 @@ class MoeSublayer:
         _check(self.lib.moe_read_stats(self.handle, ctypes.byref(st)), "moe_read_stats")
         return {"forwards": st.forwards, "launches": st.launches,
                 "stage_ms": {STAGES[i]: float(st.stage_ms[i]) for i in range(st.n_stages)}}
+
+
+# Scratch limit of moe_route_static: ceil(T / 128) * E histogram cells.
+ROUTE_STATIC_MAX_CELLS = 131072
+
+
+def route_static(logits: torch.Tensor, corr_bias: torch.Tensor, top_k: int,
+                 routed_scale: float, out: Optional[dict] = None, stream=None) -> dict:
+    """moe_route_static: routing of a batch from fp32 router logits [T, E]
+    on the current device, with no allocation inside the library (for
+    callers that cannot allocate device memory).  ``out`` may hold the
+    caller's output tensors (idx, w, counts, offsets, pos, row_tok, row_w);
+    missing ones are created here with torch.  Calls that overlap on the GPU
+    share one static scratch array and race."""
+    T, E = logits.shape
+    dev = logits.device
+    shapes = {"idx": ((T, top_k), torch.int32), "w": ((T, top_k), torch.float32),
+              "counts": ((E,), torch.int32), "offsets": ((E + 1,), torch.int32),
+              "pos": ((T, top_k), torch.int32), "row_tok": ((T * top_k,), torch.int32),
+              "row_w": ((T * top_k,), torch.float32)}
+    res = dict(out or {})
+    for name, (shape, dt) in shapes.items():
+        if name not in res:
+            res[name] = torch.empty(shape, dtype=dt, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    st = load_library().moe_route_static(
+        T, E, top_k, routed_scale, _ptr(logits), _ptr(corr_bias), _ptr(res["idx"]),
+        _ptr(res["w"]), _ptr(res["counts"]), _ptr(res["offsets"]), _ptr(res["pos"]),
+        _ptr(res["row_tok"]), _ptr(res["row_w"]), ctypes.c_void_p(stream.cuda_stream))
+    if st == MOE_ERR_UNSUPPORTED:
+        raise MoeError(st, f"moe_route_static: ceil(T/128)*E = {-(-T // 128) * E} exceeds the "
+                           f"static scratch limit of {ROUTE_STATIC_MAX_CELLS} cells")
+    _check(st, "moe_route_static")
+    return res

@@ -255,6 +255,81 @@ __global__ void topk_kernel(const float2* __restrict__ part, const float* __rest
         chunk_cnt[static_cast<size_t>(chunk) * E + e] = cnt[e];
 }
 
+// The same selection as topk_kernel, for callers that hold the router
+// logits as plain fp32 values [T, E] rather than the router's (hi, lo)
+// pairs.  Given the logits topk_kernel rounded, the two kernels take the
+// same decisions and produce the same weights bit for bit.
+template <int EPL>
+__global__ void topk_logits_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+                                   int T, int E, int k, float routed_scale,
+                                   int* __restrict__ idx_out, float* __restrict__ w_out,
+                                   int* __restrict__ chunk_cnt) {
+    extern __shared__ int cnt[];  // [E]
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int chunk = blockIdx.x;
+    for (int tl = warp; tl < CHUNK_TOKENS; tl += nw) {
+        const int t = chunk * CHUNK_TOKENS + tl;
+        if (t >= T) break;
+        float bv[EPL], sv[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) {
+                const float l = logits[static_cast<size_t>(t) * E + e];
+                const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
+                const float b = __fadd_rn(s, bias[e]);
+                sv[i] = s;
+                bv[i] = (b == b) ? b : -INFINITY;
+            } else {
+                sv[i] = 0.f;
+                bv[i] = 0.f;
+            }
+        }
+        int my_e = 0;
+        float my_s = 0.f;
+        uint32_t removed = 0u;
+        for (int j = 0; j < k; ++j) {
+            float bb = 0.f, bs = 0.f;
+            int be = -1;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E && !((removed >> i) & 1u) && (be < 0 || bv[i] > bb)) {
+                    bb = bv[i];
+                    be = e;
+                    bs = sv[i];
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ob = __shfl_xor_sync(0xffffffffu, bb, off);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+                const float os = __shfl_xor_sync(0xffffffffu, bs, off);
+                if (oe >= 0 && (be < 0 || ob > bb || (ob == bb && oe < be))) {
+                    bb = ob;
+                    be = oe;
+                    bs = os;
+                }
+            }
+            if ((be & 31) == lane) removed |= 1u << (be >> 5);
+            if (lane == j) { my_e = be; my_s = bs; }
+        }
+        float ssum = 0.f;
+        for (int j = 0; j < k; ++j) ssum = __fadd_rn(ssum, __shfl_sync(0xffffffffu, my_s, j));
+        if (lane < k) {
+            idx_out[static_cast<size_t>(t) * k + lane] = my_e;
+            w_out[static_cast<size_t>(t) * k + lane] =
+                __fdiv_rn(__fmul_rn(routed_scale, my_s), ssum);
+            atomicAdd(&cnt[my_e], 1);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        chunk_cnt[static_cast<size_t>(chunk) * E + e] = cnt[e];
+}
+
 // --------------------------------------------------- histogram scan (1 block)
 // counts[e] = sum over chunks; offsets = exclusive scan of counts (offsets[E]
 // = T*k); chunk_base[c][e] = offsets[e] + rows of expert e in chunks < c.

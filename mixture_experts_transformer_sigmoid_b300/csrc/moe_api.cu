@@ -415,7 +415,81 @@ moe_status forward_impl(moe_handle* h, const FwdArgs& a, cudaStream_t st) {
 
 }  // namespace
 
+// ------------------------------------------- routing without allocation
+// Scratch of moe_route_static: the per-chunk expert histograms and their
+// running bases, [ceil(T / 128)][E] each.  It lives in the module's static
+// device memory, so the entry point never allocates; every GPU that loads
+// the library holds these 1 MB until the process exits.  All calls on a
+// device share it, so calls that overlap on the GPU race.  Every cell a
+// call reads is written earlier in the same call, so nothing needs clearing
+// between calls.
+constexpr int ROUTE_STATIC_MAX_CELLS = 131072;  // ceil(T / 128) * E, per array
+static __device__ __align__(256) int g_route_scratch[2 * ROUTE_STATIC_MAX_CELLS];
+
+namespace {
+std::mutex g_route_scratch_mu;
+int* g_route_scratch_dev[64] = {};  // device address of g_route_scratch, per device
+
+// The symbol's device address on device `dev` (the current device).  In
+// host code g_route_scratch names a host-side stand-in, not device memory,
+// so kernels must be given this address instead.
+int* route_scratch(int dev) {
+    std::lock_guard<std::mutex> lock(g_route_scratch_mu);
+    if (g_route_scratch_dev[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess) return nullptr;
+        g_route_scratch_dev[dev] = static_cast<int*>(p);
+    }
+    return g_route_scratch_dev[dev];
+}
+
+template <int EPL>
+void launch_topk_logits_e(const float* logits, const float* bias, int T, int E, int k, float scale,
+                          int* idx, float* w, int* chunk_cnt, cudaStream_t st) {
+    const int n_chunks = (T + CHUNK_TOKENS - 1) / CHUNK_TOKENS;
+    topk_logits_kernel<EPL><<<n_chunks, 512, E * sizeof(int), st>>>(logits, bias, T, E, k, scale,
+                                                                    idx, w, chunk_cnt);
+}
+}  // namespace
+
 extern "C" {
+
+moe_status moe_route_static(int32_t T, int32_t E, int32_t top_k, float routed_scale,
+                            const float* logits, const float* corr_bias, int32_t* idx, float* w,
+                            int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* row_tok,
+                            float* row_w, void* stream) {
+    if (T < 0 || E < 1 || E > 1024 || top_k < 1 || top_k > 32 || top_k > E ||
+        !std::isfinite(routed_scale))
+        return MOE_ERR_INVALID_ARG;
+    const int64_t n_chunks = (static_cast<int64_t>(T) + CHUNK_TOKENS - 1) / CHUNK_TOKENS;
+    if (n_chunks * E > ROUTE_STATIC_MAX_CELLS) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    const void* ptrs[] = {logits, corr_bias, idx, w, counts, offsets, pos, row_tok, row_w};
+    for (const void* p : ptrs)
+        if (p == nullptr || (reinterpret_cast<uintptr_t>(p) & 3u) != 0) return MOE_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    int* scratch = route_scratch(dev);
+    if (scratch == nullptr) return MOE_ERR_CUDA;
+    int* chunk_cnt = scratch;
+    int* chunk_base = scratch + ROUTE_STATIC_MAX_CELLS;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int nch = static_cast<int>(n_chunks);
+#define MOE_TOPK_LOGITS(EPL) \
+    launch_topk_logits_e<EPL>(logits, corr_bias, T, E, top_k, routed_scale, idx, w, chunk_cnt, st)
+    if (E <= 32) MOE_TOPK_LOGITS(1);
+    else if (E <= 64) MOE_TOPK_LOGITS(2);
+    else if (E <= 128) MOE_TOPK_LOGITS(4);
+    else if (E <= 256) MOE_TOPK_LOGITS(8);
+    else if (E <= 512) MOE_TOPK_LOGITS(16);
+    else MOE_TOPK_LOGITS(32);
+#undef MOE_TOPK_LOGITS
+    scan_kernel<<<1, std::max(32, (E + 31) / 32 * 32), 0, st>>>(chunk_cnt, nch, E, counts, offsets,
+                                                               chunk_base);
+    scatter_kernel<<<nch, CHUNK_TOKENS, E * (CHUNK_TOKENS / 32) * sizeof(uint32_t), st>>>(
+        idx, w, T, E, top_k, chunk_base, pos, row_tok, row_w);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 const char* moe_status_string(moe_status s) {
     switch (s) {

@@ -114,3 +114,15 @@ def test_binding_fails_loudly_without_library(tmp_path):
             B2.load_library(str(tmp_path / "missing.so"))
     finally:
         B2._lib = saved
+
+
+@pytest.mark.parametrize("T,E,k,status", [
+    (-1, 8, 2, B.MOE_ERR_INVALID_ARG), (64, 0, 1, B.MOE_ERR_INVALID_ARG),
+    (64, 8, 0, B.MOE_ERR_INVALID_ARG), (64, 8, 9, B.MOE_ERR_INVALID_ARG),
+    (64, 2000, 2, B.MOE_ERR_INVALID_ARG), (128 * 513, 256, 8, B.MOE_ERR_UNSUPPORTED),
+    (64, 8, 2, B.MOE_ERR_INVALID_ARG),   # valid sizes, null pointers
+    (0, 8, 2, B.MOE_OK),                 # nothing to do, no pointer read
+])
+def test_route_static_host_checks(lib, T, E, k, status):
+    nulls = [None] * 9
+    assert lib.moe_route_static(T, E, k, 1.0, *nulls, None) == status
