@@ -1,0 +1,298 @@
+// Grouped GEMM on CTA pairs (tcgen05.mma.cta_group::2), for batches large
+// enough that each expert gets tens to hundreds of tokens.
+//
+// Same orientation and segments as tc_gemm_kernel (k_gemm_tc.cuh): weight
+// features on the MMA's M side, tokens on N.  Two CTAs of a cluster work on
+// one 256 x N tile: each holds 128 weight rows (its A half) and N/2 of the
+// tile's tokens (its B half); the tensor cores of the pair exchange the B
+// halves, and each CTA's tensor memory receives its 128 rows of D over all
+// N columns.  Compared with one CTA per 128 x 256 tile, a CTA stages half
+// the token bytes per k-block (32 KB stages instead of 48 KB), so the ring
+// is 6 deep instead of 4, and each token tile is read from L2 by half as
+// many CTAs.
+//
+// Roles.  Warp 0 of each CTA loads its own A and B halves; both CTAs'
+// copies count on the leader's (rank 0) `full` barrier, so the leader's
+// single MMA thread sees one barrier per stage.  The leader issues every
+// MMA and commits to the `empty` and `tfull` barriers of both CTAs at once
+// (multicast).  Warps 2-5 of each CTA drain its own tensor memory; all
+// eight epilogue warps arrive on the leader's `tempty` barrier.  Every wait
+// is bounded; a CTA that gives up sets the device error flag, and both CTAs
+// still meet at the final cluster barrier before tensor memory is freed.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "k_gemm_tc.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+constexpr int PR_BN = 256;                           // tokens per tile (MMA N, both CTAs)
+constexpr int PR_STAGES = 6;
+constexpr uint32_t PR_A_BYTES = 2 * TC_BOX_BYTES;    // 128 weight rows x 64 k
+constexpr uint32_t PR_B_BYTES = 2 * TC_BOX_BYTES;    // up to 128 token rows x 64 k
+constexpr uint32_t PR_STAGE_BYTES = PR_A_BYTES + PR_B_BYTES;
+
+struct PrSmem {
+    static constexpr uint32_t RING = PR_STAGES * PR_STAGE_BYTES;
+    static constexpr uint32_t BARS = (2 * PR_STAGES + 5) * 8;
+    static constexpr uint32_t XBUF = 64 * 33 * 4;
+    static constexpr int MAX_E = 1024;
+    static constexpr uint32_t PREFIX = (MAX_E + 4) * 4;
+    static constexpr uint32_t MISC = 32;
+    static constexpr uint32_t TOTAL = 1024 + RING + BARS + MISC + PREFIX + XBUF;
+};
+
+// Launched with a cluster dimension of 2 (cudaLaunchKernelEx).
+template <int EPI>
+__global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
+    using S = PrSmem;
+    static_assert(S::TOTAL <= 232448, "shared memory");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;                               // PR_STAGES x 16 KB
+    uint8_t* sB = smem + PR_STAGES * PR_A_BYTES;      // PR_STAGES x 16 KB
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::RING);
+    uint64_t* empty = full + PR_STAGES;
+    uint64_t* tfull = empty + PR_STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + S::RING + S::BARS);
+    uint32_t* tmem_holder = misc;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+    volatile int* epi_ok = reinterpret_cast<volatile int*>(misc + 2);
+    int* prefix = reinterpret_cast<int*>(smem + S::RING + S::BARS + S::MISC);
+    float* xbuf = reinterpret_cast<float*>(smem + S::RING + S::BARS + S::MISC + S::PREFIX);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = static_cast<int>(cluster_id_x());
+    const int n_pairs = static_cast<int>(n_clusters_x());
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PR_STAGES; ++s) {
+            mbar_init(&full[s], 1);    // the leader's expect_tx; bytes of both CTAs
+            mbar_init(&empty[s], 1);   // the leader's multicast commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 8);  // four epilogue warps in each CTA
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        for (int s = 0; s < p.n_segs; ++s) {
+            tma_prefetch_desc(&p.a0[s]);
+            tma_prefetch_desc(&p.a1[s]);
+            tma_prefetch_desc(&p.b[s]);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_holder, 2 * PR_BN);
+        tmem_relinquish_pair();
+    }
+    if (warp == 2) {
+        bool any_grouped = false;
+        for (int s = 0; s < p.n_segs; ++s) any_grouped |= (p.seg[s].grouped != 0);
+        if (any_grouped) {
+            int run = 0;
+            for (int base = 0; base < p.E; base += 32) {
+                const int e = base + lane;
+                int v = 0;
+                if (e < p.E) v = (p.offsets[e + 1] - p.offsets[e] + PR_BN - 1) / PR_BN;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int u = __shfl_up_sync(0xffffffffu, v, off);
+                    if (lane >= off) v += u;
+                }
+                if (e < p.E) prefix[e + 1] = run + v;
+                run += __shfl_sync(0xffffffffu, v, 31);
+            }
+            if (lane == 0) prefix[0] = 0;
+        }
+    }
+    tc_fence_before();
+    cluster_sync_all();   // barriers of both CTAs initialised, tensor memory allocated
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int L = pair; ok; L += n_pairs) {
+                TileInfo ti;
+                if (!decode_tile(p, prefix, L, PR_BN, ti)) break;
+                const TcSeg& sg = p.seg[ti.seg];
+                const CUtensorMap* ma0 = &p.a0[ti.seg];
+                const CUtensorMap* ma1 = &p.a1[ti.seg];
+                const CUtensorMap* mb = &p.b[ti.seg];
+                const int n = (ti.rows + 15) & ~15;        // MMA N
+                const int half = n >> 1;                   // token rows per CTA
+                const int nb = (half + 63) >> 6;           // 64-row boxes per CTA
+                const int f0 = ti.ftile * sg.a_fstride + static_cast<int>(rank) * sg.a_rank_off;
+                const int r0 = ti.row0 + static_cast<int>(rank) * half;
+                const uint32_t tx = 2u * (PR_A_BYTES + nb * TC_BOX_BYTES);
+                const int nkb = sg.K / TC_BK;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, TC_TIMEOUT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+                    if (leader) mbar_arrive_expect_tx(&full[stage], tx);
+                    uint8_t* a_dst = sA + stage * PR_A_BYTES;
+                    uint8_t* b_dst = sB + stage * PR_B_BYTES;
+                    const int k0 = kb * TC_BK;
+                    if (sg.grouped) {
+                        tma_load_3d_pair(a_dst, ma0, bar, f0, k0, ti.grp);
+                        tma_load_3d_pair(a_dst + TC_BOX_BYTES, ma1, bar, f0 + sg.a_foff1, k0, ti.grp);
+                    } else {
+                        tma_load_2d_pair(a_dst, ma0, bar, k0, f0);
+                        tma_load_2d_pair(a_dst + TC_BOX_BYTES, ma1, bar, k0, f0 + sg.a_foff1);
+                    }
+                    for (int j = 0; j < nb; ++j)
+                        tma_load_2d_pair(b_dst + j * TC_BOX_BYTES, mb, bar, k0, r0 + j * 64);
+                    if (++stage == PR_STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // let copies already issued land before the CTA moves on
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 2000000ull) {}
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (leader only)
+        if (leader && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int L = pair; ok; L += n_pairs) {
+                TileInfo ti;
+                if (!decode_tile(p, prefix, L, PR_BN, ti)) break;
+                const TcSeg& sg = p.seg[ti.seg];
+                const int n = (ti.rows + 15) & ~15;
+                const int a_mn = sg.grouped;
+                const uint32_t idesc = idesc_bf16_f32(2 * TC_BM, n, a_mn, 0);
+                if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, TC_TIMEOUT_NS)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PR_BN);
+                const int nkb = sg.K / TC_BK;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, TC_TIMEOUT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sA + stage * PR_A_BYTES);
+                    const uint32_t b_addr = smem_u32(sB + stage * PR_B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < TC_BK / TC_UMMA_K; ++kk) {
+                        // descriptors as in tc_gemm_kernel; the peer's halves sit at
+                        // the same shared-memory offsets
+                        const uint64_t ad = a_mn ? sdesc_sw128(a_addr + kk * 2048, TC_BOX_BYTES, 1024)
+                                                 : sdesc_sw128(a_addr + kk * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(b_addr + kk * 32, 16, 1024);
+                        tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc_commit_pair(&empty[stage], 0x3);
+                    if (++stage == PR_STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit_pair(&tfull[acc], 0x3);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            tc_commit_pair(drain, 0x1);
+            mbar_wait(drain, 0, nullptr, ok ? TC_TIMEOUT_NS : TC_DRAIN_NS);
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2-5, both CTAs)
+        const int q = warp & 3;
+        const int et = threadIdx.x - 64;
+        const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
+        const uint32_t tempty_leader1 = mapa_shared(smem_u32(&tempty[1]), 0);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int it = 0;
+        for (int L = pair;; L += n_pairs, ++it) {
+            TileInfo ti;
+            if (!decode_tile(p, prefix, L, PR_BN, ti)) break;
+            if (et == 0)
+                epi_ok[it & 1] = mbar_wait(&tfull[acc], acc_phase, abort_flag, TC_TIMEOUT_NS) ? 1 : 0;
+            named_bar_sync(1, 128);
+            if (!epi_ok[it & 1]) break;
+            tc_fence_after();
+            const TcSeg& sg = p.seg[ti.seg];
+            const int fbase = ti.ftile * sg.a_fstride + static_cast<int>(rank) * sg.a_rank_off;
+            const uint32_t t_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                    static_cast<uint32_t>(acc * PR_BN);
+            for (int c0 = 0; c0 < ti.rows; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(t_base + c0, v);
+                tmem_ld_wait();
+                if constexpr (EPI == EPI_SWIGLU) {
+                    if (q >= 2) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            xbuf[((q - 2) * 32 + lane) * 33 + c] = __uint_as_float(v[c]);
+                    }
+                    named_bar_sync(2, 128);
+                    if (q < 2) {
+                        const int col = fbase + q * 32 + lane;
+                        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
+                        if (col < sg.F) {
+                            const int cmax = min(32, ti.rows - c0);
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) {
+                                if (c >= cmax) break;
+                                const float g = __uint_as_float(v[c]);
+                                const float u = xbuf[(q * 32 + lane) * 33 + c];
+                                const float hv = g / (1.0f + __expf(-g)) * u;
+                                out[static_cast<size_t>(ti.row0 + c0 + c) * sg.ld_out + col] =
+                                    __float2bfloat16_rn(hv);
+                            }
+                        }
+                    }
+                    named_bar_sync(2, 128);
+                } else if constexpr (EPI == EPI_WEIGHTED) {
+                    const int col = fbase + q * 32 + lane;
+                    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
+                    if (col < sg.F) {
+                        const int cmax = min(32, ti.rows - c0);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            if (c >= cmax) break;
+                            const int row = ti.row0 + c0 + c;
+                            const float wv = sg.row_w ? sg.row_w[row] : 1.0f;
+                            out[static_cast<size_t>(row) * sg.ld_out + col] =
+                                __float2bfloat16_rn(__uint_as_float(v[c]) * wv);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            if (lane == 0) mbar_arrive_cluster(acc == 0 ? tempty_leader0 : tempty_leader1);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync_all();   // no CTA frees tensor memory or exits while its peer may still signal it
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, 2 * PR_BN);
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(p.err, DEVERR_TIMEOUT);
+}
+
+}  // namespace moe

@@ -59,6 +59,7 @@ struct TcSeg {
     int ld_out;           // output row stride in elements
     void* out;            // bf16 output [rows, ld_out]
     const float* row_w;   // weighted epilogue: per-row factor; null means 1
+    int a_rank_off;       // CTA-pair kernel: feature offset of the second CTA's rows
 };
 
 struct TcParams {

@@ -22,6 +22,7 @@
 #include <type_traits>
 #include <vector>
 
+#include "k_gemm_pair.cuh"
 #include "k_gemm_tc.cuh"
 #include "k_route.cuh"
 #include "k_router_tc.cuh"
@@ -179,10 +180,47 @@ int tile_bound(const TcParams& prm, int BN, int P) {
     return static_cast<int>(std::min<int64_t>(n, 1 << 30));
 }
 
+// CTA-pair grouped GEMM: as many clusters of two as the device keeps
+// resident at once (the tile schedule is static, so every launched cluster
+// must run from the start), at most one per tile.
 template <int EPI>
-cudaError_t run_tc(const TcParams& prm, int BN, int P, int num_sms, cudaStream_t st) {
-    const int grid = std::max(1, std::min(num_sms, tile_bound(prm, BN, P)));
-    if (BN == 256) return launch_tc<256, 4, EPI>(prm, grid, st);
+cudaError_t launch_pair(const TcParams& prm, int P, int num_sms, cudaStream_t st) {
+    static int max_clusters[64] = {};  // per device, found before the first launch
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64) return cudaErrorInvalidDevice;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(TC_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = PrSmem::TOTAL;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (max_clusters[dev] == 0) {
+        e = cudaFuncSetAttribute(tc_gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PrSmem::TOTAL);
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3(std::max(2, num_sms / 2 * 2), 1, 1);
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<EPI>, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        max_clusters[dev] = n;
+    }
+    const int clusters = std::max(1, std::min(max_clusters[dev], tile_bound(prm, PR_BN, P)));
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<EPI>, prm);
+}
+
+template <int EPI>
+cudaError_t run_tc(const TcParams& prm, bool pair, int P, int num_sms, cudaStream_t st) {
+    if (pair) return launch_pair<EPI>(prm, P, num_sms, st);
+    const int grid = std::max(1, std::min(num_sms, tile_bound(prm, 64, P)));
     return launch_tc<64, 8, EPI>(prm, grid, st);
 }
 
@@ -298,7 +336,9 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     T* hs = static_cast<T*>(h->hs);
     T* sh = Is > 0 ? static_cast<T*>(h->sh) : nullptr;
     if (h->tc) {
-        const int BN = (P >= 64 * E) ? 256 : 64;
+        // CTA pairs (256 x 256 tiles) once experts average 64 tokens or more;
+        // below that the single-CTA kernel with 64-token tiles wastes less.
+        const bool pair = P >= 64 * E;
         // F+H(gate/up): routed + shared gate|up with SwiGLU epilogue
         TcParams g1;
         std::memset(&g1, 0, sizeof g1);
@@ -309,14 +349,16 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
         if (!map_3d(&g1.a0[0], a.gate_up, 2 * I, d, E) || !map_3d(&g1.a1[0], a.gate_up, 2 * I, d, E) ||
             !map_2d(&g1.b[0], h->xp, d, P))
             return MOE_ERR_CUDA;
-        g1.seg[0] = TcSeg{1, 0, d, 64, I, I / 64, I, I, hbuf, nullptr};
+        g1.seg[0] = pair ? TcSeg{1, 0, d, 128, I, (I + 127) / 128, I, I, hbuf, nullptr, 64}
+                         : TcSeg{1, 0, d, 64, I, I / 64, I, I, hbuf, nullptr, 0};
         if (Is > 0) {
             if (!map_2d(&g1.a0[1], a.sg, d, Is) || !map_2d(&g1.a1[1], a.su, d, Is) ||
                 !map_2d(&g1.b[1], xn, d, Tn))
                 return MOE_ERR_CUDA;
-            g1.seg[1] = TcSeg{0, Tn, d, 64, 0, Is / 64, Is, Is, hs, nullptr};
+            g1.seg[1] = pair ? TcSeg{0, Tn, d, 128, 0, (Is + 127) / 128, Is, Is, hs, nullptr, 64}
+                             : TcSeg{0, Tn, d, 64, 0, Is / 64, Is, Is, hs, nullptr, 0};
         }
-        if (run_tc<EPI_SWIGLU>(g1, BN, P, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        if (run_tc<EPI_SWIGLU>(g1, pair, P, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
         mark(h, 7, st);
         // G+H(down): routed down with routing weight + shared down
         TcParams g2;
@@ -328,14 +370,16 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
         if (!map_3d(&g2.a0[0], a.down, d, I, E) || !map_3d(&g2.a1[0], a.down, d, I, E) ||
             !map_2d(&g2.b[0], hbuf, I, P))
             return MOE_ERR_CUDA;
-        g2.seg[0] = TcSeg{1, 0, I, 128, 64, (d + 127) / 128, d, d, yp, h->row_w};
+        g2.seg[0] = pair ? TcSeg{1, 0, I, 256, 64, (d + 255) / 256, d, d, yp, h->row_w, 128}
+                         : TcSeg{1, 0, I, 128, 64, (d + 127) / 128, d, d, yp, h->row_w, 0};
         if (Is > 0) {
             if (!map_2d(&g2.a0[1], a.sd, Is, d) || !map_2d(&g2.a1[1], a.sd, Is, d) ||
                 !map_2d(&g2.b[1], hs, Is, Tn))
                 return MOE_ERR_CUDA;
-            g2.seg[1] = TcSeg{0, Tn, Is, 128, 64, (d + 127) / 128, d, d, sh, nullptr};
+            g2.seg[1] = pair ? TcSeg{0, Tn, Is, 256, 64, (d + 255) / 256, d, d, sh, nullptr, 128}
+                             : TcSeg{0, Tn, Is, 128, 64, (d + 127) / 128, d, d, sh, nullptr, 0};
         }
-        if (run_tc<EPI_WEIGHTED>(g2, BN, P, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        if (run_tc<EPI_WEIGHTED>(g2, pair, P, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
         h->launches += 2;
     } else {
         const T* gu = static_cast<const T*>(a.gate_up);
