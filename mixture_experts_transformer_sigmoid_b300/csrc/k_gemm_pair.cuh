@@ -45,6 +45,46 @@ struct PrSmem {
     static constexpr uint32_t TOTAL = 1024 + RING + BARS + MISC + PREFIX + XBUF;
 };
 
+// Position of a CTA's producer in its sequence of (tile, k-block) loads, with
+// the coordinates of the CTA's half of the tile.
+// How a CTA's 128 A rows arrive, one k-block at a time (16 KB either way).
+enum PairAKind {
+    PA_TWO_2D = 0,      // two 64-row boxes of K-major maps: a0 at row f0, a1 at row f0 + a_foff1
+    PA_ONE_2D = 1,      // one 128-row box of the K-major map a0 at row f0
+    PA_HALVES_4D = 2,   // grouped gate|up: 4-D map {feature, k, half, expert}, both halves at f0
+    PA_CHUNKS_4D = 3    // grouped down: 4-D map {feature, k, 64-feature chunk, expert}, chunks f0/64 and f0/64 + 1
+};
+
+struct PairCursor {
+    int L, kb, nkb;
+    int f0;      // first feature of this CTA's A rows
+    int r0;      // first token row of this CTA's B half
+    int nb;      // B bytes this CTA loads per k-block, in 8 KB units (one 64- or 128-row box)
+    bool valid;
+    TileInfo ti;
+
+    __device__ void set_tile(const TcParams& p, const int* prefix, uint32_t rank) {
+        valid = decode_tile(p, prefix, L, PR_BN, ti);
+        if (!valid) return;
+        const TcSeg& sg = p.seg[ti.seg];
+        const int half = ((ti.rows + 15) & ~15) >> 1;  // MMA N / 2
+        nb = half > 64 ? 2 : 1;
+        f0 = ti.ftile * sg.a_fstride + static_cast<int>(rank) * sg.a_rank_off;
+        r0 = ti.row0 + static_cast<int>(rank) * half;
+        nkb = sg.K / TC_BK;
+        kb = 0;
+    }
+    __device__ void start(const TcParams& p, const int* prefix, int first, uint32_t rank) {
+        L = first;
+        set_tile(p, prefix, rank);
+    }
+    __device__ void advance(const TcParams& p, const int* prefix, int stride, uint32_t rank) {
+        if (++kb < nkb) return;
+        L += stride;
+        set_tile(p, prefix, rank);
+    }
+};
+
 // Launched with a cluster dimension of 2 (cudaLaunchKernelEx).
 template <int EPI>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
@@ -89,6 +129,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_pair_kernel(const __gri
             tma_prefetch_desc(&p.a0[s]);
             tma_prefetch_desc(&p.a1[s]);
             tma_prefetch_desc(&p.b[s]);
+            tma_prefetch_desc(&p.b128[s]);
         }
     }
     if (warp == 1) {
@@ -122,45 +163,44 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_pair_kernel(const __gri
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
+        // One A load (16 KB) and one B load (8 or 16 KB) per k-block: the TMA
+        // unit's cost grows with the number of copies, not only their bytes.
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int L = pair; ok; L += n_pairs) {
-                TileInfo ti;
-                if (!decode_tile(p, prefix, L, PR_BN, ti)) break;
-                const TcSeg& sg = p.seg[ti.seg];
-                const CUtensorMap* ma0 = &p.a0[ti.seg];
-                const CUtensorMap* ma1 = &p.a1[ti.seg];
-                const CUtensorMap* mb = &p.b[ti.seg];
-                const int n = (ti.rows + 15) & ~15;        // MMA N
-                const int half = n >> 1;                   // token rows per CTA
-                const int nb = (half + 63) >> 6;           // 64-row boxes per CTA
-                const int f0 = ti.ftile * sg.a_fstride + static_cast<int>(rank) * sg.a_rank_off;
-                const int r0 = ti.row0 + static_cast<int>(rank) * half;
-                const uint32_t tx = 2u * (PR_A_BYTES + nb * TC_BOX_BYTES);
-                const int nkb = sg.K / TC_BK;
-                for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, TC_TIMEOUT_NS)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
-                    if (leader) mbar_arrive_expect_tx(&full[stage], tx);
-                    uint8_t* a_dst = sA + stage * PR_A_BYTES;
-                    uint8_t* b_dst = sB + stage * PR_B_BYTES;
-                    const int k0 = kb * TC_BK;
-                    if (sg.grouped) {
-                        tma_load_3d_pair(a_dst, ma0, bar, f0, k0, ti.grp);
-                        tma_load_3d_pair(a_dst + TC_BOX_BYTES, ma1, bar, f0 + sg.a_foff1, k0, ti.grp);
-                    } else {
-                        tma_load_2d_pair(a_dst, ma0, bar, k0, f0);
-                        tma_load_2d_pair(a_dst + TC_BOX_BYTES, ma1, bar, k0, f0 + sg.a_foff1);
-                    }
-                    for (int j = 0; j < nb; ++j)
-                        tma_load_2d_pair(b_dst + j * TC_BOX_BYTES, mb, bar, k0, r0 + j * 64);
-                    if (++stage == PR_STAGES) { stage = 0; phase ^= 1u; }
+            PairCursor ld;
+            ld.start(p, prefix, pair, rank);
+            while (ld.valid) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, TC_TIMEOUT_NS)) {
+                    ok = false;
+                    break;
                 }
+                const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+                if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (PR_A_BYTES + ld.nb * TC_BOX_BYTES));
+                uint8_t* a_dst = sA + stage * PR_A_BYTES;
+                uint8_t* b_dst = sB + stage * PR_B_BYTES;
+                const int sgi = ld.ti.seg;
+                const TcSeg& sg = p.seg[sgi];
+                const int k0 = ld.kb * TC_BK;
+                switch (sg.a_kind) {
+                    case PA_TWO_2D:
+                        tma_load_2d_pair(a_dst, &p.a0[sgi], bar, k0, ld.f0);
+                        tma_load_2d_pair(a_dst + TC_BOX_BYTES, &p.a1[sgi], bar, k0, ld.f0 + sg.a_foff1);
+                        break;
+                    case PA_ONE_2D:
+                        tma_load_2d_pair(a_dst, &p.a0[sgi], bar, k0, ld.f0);
+                        break;
+                    case PA_HALVES_4D:
+                        tma_load_4d_pair(a_dst, &p.a0[sgi], bar, ld.f0, k0, 0, ld.ti.grp);
+                        break;
+                    default:
+                        tma_load_4d_pair(a_dst, &p.a0[sgi], bar, 0, k0, ld.f0 >> 6, ld.ti.grp);
+                        break;
+                }
+                tma_load_2d_pair(b_dst, ld.nb == 2 ? &p.b128[sgi] : &p.b[sgi], bar, k0, ld.r0);
+                if (++stage == PR_STAGES) { stage = 0; phase ^= 1u; }
+                ld.advance(p, prefix, n_pairs, rank);
             }
             if (!ok) {
                 // let copies already issued land before the CTA moves on

@@ -60,12 +60,14 @@ struct TcSeg {
     void* out;            // bf16 output [rows, ld_out]
     const float* row_w;   // weighted epilogue: per-row factor; null means 1
     int a_rank_off;       // CTA-pair kernel: feature offset of the second CTA's rows
+    int a_kind;           // CTA-pair kernel: how a0 delivers the 128 A rows (PairAKind)
 };
 
 struct TcParams {
     CUtensorMap a0[2];    // per segment: map of the first A box
     CUtensorMap a1[2];    // per segment: map of the second A box
     CUtensorMap b[2];     // per segment: map of B ([rows, K], K contiguous)
+    CUtensorMap b128[2];  // CTA-pair kernel: the same B with 128-row boxes
     TcSeg seg[2];
     int n_segs;
     int E;                // groups of the grouped segment

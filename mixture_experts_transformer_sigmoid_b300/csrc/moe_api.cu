@@ -89,13 +89,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return g_encode;
 }
 
-// bf16 tensor [outer][inner] (inner contiguous), 64 x 64 boxes, 128-byte swizzle.
-bool map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+// bf16 tensor [outer][inner] (inner contiguous), 64 x box_rows boxes, 128-byte swizzle.
+bool map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_rows = 64) {
     auto enc = encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {64, 64};
+    cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -110,6 +110,25 @@ bool map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint
     cuuint32_t box[3] = {64, 64, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Grouped bf16 weights read as two 64-feature x 64-k boxes per copy: a 4-D
+// view {feature (f_extent, contiguous), k (k_extent rows, k_stride bytes),
+// chunk (n_chunks, chunk_stride bytes), group (groups, group_stride bytes)},
+// box {64, 64, 2, 1}.  The copy lands as chunk 0 then chunk 1, each 64 k
+// rows of 128 swizzled bytes: the layout of two separate 64 x 64 boxes.
+bool map_4d_chunks(CUtensorMap* m, const void* base, uint64_t f_extent, uint64_t k_extent,
+                   uint64_t k_stride, uint64_t n_chunks, uint64_t chunk_stride, uint64_t groups,
+                   uint64_t group_stride) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {f_extent, k_extent, n_chunks, groups};
+    cuuint64_t strides[3] = {k_stride, chunk_stride, group_stride};
+    cuuint32_t box[4] = {64, 64, 2, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -346,17 +365,25 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
         g1.offsets = h->offsets;
         g1.err = h->err;
         g1.n_segs = Is > 0 ? 2 : 1;
-        if (!map_3d(&g1.a0[0], a.gate_up, 2 * I, d, E) || !map_3d(&g1.a1[0], a.gate_up, 2 * I, d, E) ||
-            !map_2d(&g1.b[0], h->xp, d, P))
-            return MOE_ERR_CUDA;
-        g1.seg[0] = pair ? TcSeg{1, 0, d, 128, I, (I + 127) / 128, I, I, hbuf, nullptr, 64}
-                         : TcSeg{1, 0, d, 64, I, I / 64, I, I, hbuf, nullptr, 0};
+        const uint64_t I2 = 2ull * I;
+        if (pair) {
+            // gate and up halves of 64 features in one copy: {f < I, k, half (stride I), expert}
+            if (!map_4d_chunks(&g1.a0[0], a.gate_up, I, d, I2 * 2, 2, uint64_t(I) * 2, E, d * I2 * 2) ||
+                !map_2d(&g1.b[0], h->xp, d, P) || !map_2d(&g1.b128[0], h->xp, d, P, 128))
+                return MOE_ERR_CUDA;
+            g1.seg[0] = TcSeg{1, 0, d, 128, I, (I + 127) / 128, I, I, hbuf, nullptr, 64, PA_HALVES_4D};
+        } else {
+            if (!map_3d(&g1.a0[0], a.gate_up, I2, d, E) || !map_3d(&g1.a1[0], a.gate_up, I2, d, E) ||
+                !map_2d(&g1.b[0], h->xp, d, P))
+                return MOE_ERR_CUDA;
+            g1.seg[0] = TcSeg{1, 0, d, 64, I, I / 64, I, I, hbuf, nullptr, 0, 0};
+        }
         if (Is > 0) {
             if (!map_2d(&g1.a0[1], a.sg, d, Is) || !map_2d(&g1.a1[1], a.su, d, Is) ||
-                !map_2d(&g1.b[1], xn, d, Tn))
+                !map_2d(&g1.b[1], xn, d, Tn) || !map_2d(&g1.b128[1], xn, d, Tn, 128))
                 return MOE_ERR_CUDA;
-            g1.seg[1] = pair ? TcSeg{0, Tn, d, 128, 0, (Is + 127) / 128, Is, Is, hs, nullptr, 64}
-                             : TcSeg{0, Tn, d, 64, 0, Is / 64, Is, Is, hs, nullptr, 0};
+            g1.seg[1] = pair ? TcSeg{0, Tn, d, 128, 0, (Is + 127) / 128, Is, Is, hs, nullptr, 64, PA_TWO_2D}
+                             : TcSeg{0, Tn, d, 64, 0, Is / 64, Is, Is, hs, nullptr, 0, 0};
         }
         if (run_tc<EPI_SWIGLU>(g1, pair, P, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
         mark(h, 7, st);
@@ -367,17 +394,32 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
         g2.offsets = h->offsets;
         g2.err = h->err;
         g2.n_segs = Is > 0 ? 2 : 1;
-        if (!map_3d(&g2.a0[0], a.down, d, I, E) || !map_3d(&g2.a1[0], a.down, d, I, E) ||
-            !map_2d(&g2.b[0], hbuf, I, P))
-            return MOE_ERR_CUDA;
-        g2.seg[0] = pair ? TcSeg{1, 0, I, 256, 64, (d + 255) / 256, d, d, yp, h->row_w, 128}
-                         : TcSeg{1, 0, I, 128, 64, (d + 127) / 128, d, d, yp, h->row_w, 0};
-        if (Is > 0) {
-            if (!map_2d(&g2.a0[1], a.sd, Is, d) || !map_2d(&g2.a1[1], a.sd, Is, d) ||
-                !map_2d(&g2.b[1], hs, Is, Tn))
+        if (pair) {
+            // two consecutive 64-feature chunks in one copy: {f < 64, k, chunk (stride 128 B), expert}
+            if (!map_4d_chunks(&g2.a0[0], a.down, 64, I, uint64_t(d) * 2, d / 64, 128, E,
+                               uint64_t(I) * d * 2) ||
+                !map_2d(&g2.b[0], hbuf, I, P) || !map_2d(&g2.b128[0], hbuf, I, P, 128))
                 return MOE_ERR_CUDA;
-            g2.seg[1] = pair ? TcSeg{0, Tn, Is, 256, 64, (d + 255) / 256, d, d, sh, nullptr, 128}
-                             : TcSeg{0, Tn, Is, 128, 64, (d + 127) / 128, d, d, sh, nullptr, 0};
+            g2.seg[0] = TcSeg{1, 0, I, 256, 64, (d + 255) / 256, d, d, yp, h->row_w, 128, PA_CHUNKS_4D};
+        } else {
+            if (!map_3d(&g2.a0[0], a.down, d, I, E) || !map_3d(&g2.a1[0], a.down, d, I, E) ||
+                !map_2d(&g2.b[0], hbuf, I, P))
+                return MOE_ERR_CUDA;
+            g2.seg[0] = TcSeg{1, 0, I, 128, 64, (d + 127) / 128, d, d, yp, h->row_w, 0, 0};
+        }
+        if (Is > 0) {
+            if (pair) {
+                // 128 consecutive nn.Linear rows of the shared down projection in one copy
+                if (!map_2d(&g2.a0[1], a.sd, Is, d, 128) || !map_2d(&g2.b[1], hs, Is, Tn) ||
+                    !map_2d(&g2.b128[1], hs, Is, Tn, 128))
+                    return MOE_ERR_CUDA;
+                g2.seg[1] = TcSeg{0, Tn, Is, 256, 64, (d + 255) / 256, d, d, sh, nullptr, 128, PA_ONE_2D};
+            } else {
+                if (!map_2d(&g2.a0[1], a.sd, Is, d) || !map_2d(&g2.a1[1], a.sd, Is, d) ||
+                    !map_2d(&g2.b[1], hs, Is, Tn))
+                    return MOE_ERR_CUDA;
+                g2.seg[1] = TcSeg{0, Tn, Is, 128, 64, (d + 127) / 128, d, d, sh, nullptr, 0, 0};
+            }
         }
         if (run_tc<EPI_WEIGHTED>(g2, pair, P, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
         h->launches += 2;
