@@ -38,7 +38,9 @@ constexpr uint32_t PR_STAGE_BYTES = PR_A_BYTES + PR_B_BYTES;
 struct PrSmem {
     static constexpr uint32_t RING = PR_STAGES * PR_STAGE_BYTES;
     static constexpr uint32_t BARS = (2 * PR_STAGES + 5) * 8;
-    static constexpr uint32_t XBUF = 64 * 33 * 4;
+    // epilogue staging: SwiGLU gate and up as [32 tokens][65] fp32 each; the
+    // weighted epilogue uses 4 warps x [32 tokens][33] fp32
+    static constexpr uint32_t XBUF = 2 * 32 * 65 * 4 + 256;
     static constexpr int MAX_E = 1024;
     static constexpr uint32_t PREFIX = (MAX_E + 4) * 4;
     static constexpr uint32_t MISC = 32;
@@ -282,44 +284,67 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_pair_kernel(const __gri
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(t_base + c0, v);
                 tmem_ld_wait();
+                const int cmax = min(32, ti.rows - c0);
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
                 if constexpr (EPI == EPI_SWIGLU) {
-                    if (q >= 2) {
+                    // lanes 0-63 of tensor memory hold gate, 64-127 up, for the same 64
+                    // features: stage both as [token][feature], then each warp takes 8
+                    // tokens and writes 8 features of one token per 16-byte store
+                    float* gs = xbuf;
+                    float* us = xbuf + 32 * 65;
+                    float* dst = q < 2 ? gs : us;
+                    const int f = (q & 1) * 32 + lane;
 #pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            xbuf[((q - 2) * 32 + lane) * 33 + c] = __uint_as_float(v[c]);
-                    }
+                    for (int c = 0; c < 32; ++c) dst[c * 65 + f] = __uint_as_float(v[c]);
                     named_bar_sync(2, 128);
-                    if (q < 2) {
-                        const int col = fbase + q * 32 + lane;
-                        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
-                        if (col < sg.F) {
-                            const int cmax = min(32, ti.rows - c0);
+                    const int t = (warp - 2) * 8 + (lane >> 2);   // token of this lane (bank = t + 8 * sub)
 #pragma unroll
-                            for (int c = 0; c < 32; ++c) {
-                                if (c >= cmax) break;
-                                const float g = __uint_as_float(v[c]);
-                                const float u = xbuf[(q * 32 + lane) * 33 + c];
-                                const float hv = g / (1.0f + __expf(-g)) * u;
-                                out[static_cast<size_t>(ti.row0 + c0 + c) * sg.ld_out + col] =
-                                    __float2bfloat16_rn(hv);
+                    for (int pass = 0; pass < 2; ++pass) {
+                        const int sub = pass * 4 + (lane & 3);     // 8-feature chunk of the 64
+                        const int col = fbase + sub * 8;
+                        if (t < cmax && col < sg.F) {
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float g0 = gs[t * 65 + sub * 8 + 2 * j], g1 = gs[t * 65 + sub * 8 + 2 * j + 1];
+                                const float u0 = us[t * 65 + sub * 8 + 2 * j], u1 = us[t * 65 + sub * 8 + 2 * j + 1];
+                                const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
+                                const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+                                const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
+                                pk[j] = *reinterpret_cast<const uint32_t*>(&hb);
                             }
+                            *reinterpret_cast<uint4*>(out + static_cast<size_t>(ti.row0 + c0 + t) * sg.ld_out + col) =
+                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
                         }
                     }
                     named_bar_sync(2, 128);
                 } else if constexpr (EPI == EPI_WEIGHTED) {
-                    const int col = fbase + q * 32 + lane;
-                    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
-                    if (col < sg.F) {
-                        const int cmax = min(32, ti.rows - c0);
+                    // stage this warp's 32 features x 32 tokens, then write 8 features of
+                    // one token per 16-byte store, scaled by that token's routing weight
+                    float* stg = xbuf + q * (32 * 33);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            if (c >= cmax) break;
-                            const int row = ti.row0 + c0 + c;
+                    for (int c = 0; c < 32; ++c) stg[c * 33 + lane] = __uint_as_float(v[c]);
+                    __syncwarp();
+                    const int sub = lane & 3;
+                    const int col = fbase + q * 32 + sub * 8;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int t = r * 8 + (lane >> 2);       // bank = t + 8 * sub: conflict-free
+                        if (t < cmax && col < sg.F) {
+                            const int row = ti.row0 + c0 + t;
                             const float wv = sg.row_w ? sg.row_w[row] : 1.0f;
-                            out[static_cast<size_t>(row) * sg.ld_out + col] =
-                                __float2bfloat16_rn(__uint_as_float(v[c]) * wv);
+                            uint32_t pk[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const __nv_bfloat162 hb = __floats2bfloat162_rn(
+                                    stg[t * 33 + sub * 8 + 2 * j] * wv, stg[t * 33 + sub * 8 + 2 * j + 1] * wv);
+                                pk[j] = *reinterpret_cast<const uint32_t*>(&hb);
+                            }
+                            *reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * sg.ld_out + col) =
+                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
                         }
                     }
+                    __syncwarp();
                 }
             }
             tc_fence_before();
