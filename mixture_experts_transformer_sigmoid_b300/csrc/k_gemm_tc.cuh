@@ -82,6 +82,9 @@ struct TileInfo {
 // Linear tile id -> (segment, group, first row, rows, feature tile).  Tiles
 // are ordered segment-major, then token tile, then feature tile, so CTAs that
 // run at the same time share the B tile and the L2 lines of the same expert.
+// A group of m rows is split evenly into ceil(m / BN) token tiles (e.g. 300
+// rows as 150 + 150, not 256 + 44): the same weight traffic, but no MMA with
+// a small N, whose fixed cost per instruction would dominate.
 __device__ __forceinline__ bool decode_tile(const TcParams& p, const int* prefix, int L, int BN,
                                             TileInfo& ti) {
     for (int s = 0; s < p.n_segs; ++s) {
@@ -99,13 +102,16 @@ __device__ __forceinline__ bool decode_tile(const TcParams& p, const int* prefix
                     if (prefix[mid] <= tt) lo = mid; else hi = mid;
                 }
                 ti.grp = lo;
-                const int r0 = p.offsets[lo] + (tt - prefix[lo]) * BN;
-                ti.row0 = r0;
-                ti.rows = min(BN, p.offsets[lo + 1] - r0);
+                const int m = p.offsets[lo + 1] - p.offsets[lo];
+                const int ntt = prefix[lo + 1] - prefix[lo];
+                const int j = tt - prefix[lo];
+                ti.row0 = p.offsets[lo] + static_cast<int>(static_cast<int64_t>(j) * m / ntt);
+                ti.rows = p.offsets[lo] + static_cast<int>(static_cast<int64_t>(j + 1) * m / ntt) - ti.row0;
             } else {
+                const int m = sg.n_rows;
                 ti.grp = 0;
-                ti.row0 = tt * BN;
-                ti.rows = min(BN, sg.n_rows - ti.row0);
+                ti.row0 = static_cast<int>(static_cast<int64_t>(tt) * m / ntok);
+                ti.rows = static_cast<int>(static_cast<int64_t>(tt + 1) * m / ntok) - ti.row0;
             }
             return true;
         }
