@@ -109,7 +109,11 @@ __device__ __forceinline__ float row_rrms(const T* xr, int d, float eps, float2*
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
 }
 
-// xn = gain * cast(x * r): one block per token.
+// xn = gain * cast(x * r): one block per token.  Rows of up to
+// RMS_REG_VECS vectors per thread stay in registers between the reduction
+// and the scaling (x is read once); longer rows are read twice.
+constexpr int RMS_REG_VECS = 4;
+
 template <typename T>
 __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ gain,
                                T* __restrict__ xn, int d, float eps) {
@@ -117,14 +121,53 @@ __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ ga
     constexpr int V = Elem<T>::V;
     const size_t t = blockIdx.x;
     const T* xr = x + t * d;
-    const float r = row_rrms<T>(xr, d, eps, red);
-    for (int v = threadIdx.x; v < d / V; v += blockDim.x) {
-        float f[V], g[V];
-        load_vec<T>(xr + v * V, f);
+    const int nvec = d / V;
+    if (nvec > RMS_REG_VECS * static_cast<int>(blockDim.x)) {
+        const float r = row_rrms<T>(xr, d, eps, red);
+        for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+            float f[V], g[V];
+            load_vec<T>(xr + v * V, f);
+            load_vec<T>(gain + v * V, g);
+#pragma unroll
+            for (int i = 0; i < V; ++i) f[i] = __fmul_rn(g[i], Elem<T>::round_io(__fmul_rn(f[i], r)));
+            store_vec<T>(xn + t * d + v * V, f);
+        }
+        return;
+    }
+    float f[RMS_REG_VECS][V];
+#pragma unroll
+    for (int j = 0; j < RMS_REG_VECS; ++j) {
+        const int v = threadIdx.x + j * blockDim.x;
+        if (v < nvec) load_vec<T>(xr + v * V, f[j]);
+    }
+    // the same compensated sum of squares as row_rrms, over the registers
+    float hi = 0.f, lo = 0.f;
+#pragma unroll
+    for (int j = 0; j < RMS_REG_VECS; ++j) {
+        if (threadIdx.x + j * blockDim.x >= nvec) continue;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const float p = __fmul_rn(f[j][i], f[j][i]);
+            const float pe = fmaf(f[j][i], f[j][i], -p);
+            float s, e;
+            two_sum_f(hi, p, s, e);
+            hi = s;
+            lo = __fadd_rn(lo, __fadd_rn(e, pe));
+        }
+    }
+    block_sum_pair(hi, lo, red);
+    const float ms = static_cast<float>((static_cast<double>(hi) + static_cast<double>(lo)) /
+                                        static_cast<double>(d));
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+#pragma unroll
+    for (int j = 0; j < RMS_REG_VECS; ++j) {
+        const int v = threadIdx.x + j * blockDim.x;
+        if (v >= nvec) continue;
+        float g[V];
         load_vec<T>(gain + v * V, g);
 #pragma unroll
-        for (int i = 0; i < V; ++i) f[i] = __fmul_rn(g[i], Elem<T>::round_io(__fmul_rn(f[i], r)));
-        store_vec<T>(xn + t * d + v * V, f);
+        for (int i = 0; i < V; ++i) f[j][i] = __fmul_rn(g[i], Elem<T>::round_io(__fmul_rn(f[j][i], r)));
+        store_vec<T>(xn + t * d + v * V, f[j]);
     }
 }
 
@@ -417,7 +460,17 @@ __global__ void gather_rows_kernel(const T* __restrict__ xn, const int* __restri
         const int t = min(max(row_tok[row], 0), n_tok - 1);
         const int4* src = reinterpret_cast<const int4*>(xn + static_cast<size_t>(t) * d);
         int4* dst = reinterpret_cast<int4*>(xp + static_cast<size_t>(row) * d);
-        for (int v = lane; v < nvec; v += 32) dst[v] = src[v];
+        // eight 16-byte loads in flight per lane before the stores
+        constexpr int U = 8;
+        int v = lane;
+        for (; v + 32 * (U - 1) < nvec; v += 32 * U) {
+            int4 r[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) r[u] = __ldg(src + v + 32 * u);
+#pragma unroll
+            for (int u = 0; u < U; ++u) dst[v + 32 * u] = r[u];
+        }
+        for (; v < nvec; v += 32) dst[v] = __ldg(src + v);
     }
 }
 

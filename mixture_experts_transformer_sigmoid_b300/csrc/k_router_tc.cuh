@@ -4,10 +4,12 @@
 // A tensor-core accumulation chained over the whole hidden size (hundreds of
 // MMAs into one fp32 accumulator) carries a rounding error that grows with
 // the chain and can exceed the top-k margins the routing must resolve
-// (biased-score gaps down to 1e-5).  So every 64-deep k-block (4 MMAs)
-// starts a fresh accumulator in tensor memory, and the epilogue warps add
-// the k-block results into a compensated (hi, lo) fp32 pair with an
-// error-free two-sum.  The bf16 x bf16 products themselves are exact.
+// (biased-score gaps down to 1e-5).  So every RT_CHAIN k-blocks of 64 (8
+// MMAs) start a fresh accumulator in tensor memory, and the epilogue warps
+// add the chain results into a compensated (hi, lo) fp32 pair with an
+// error-free two-sum.  The bf16 x bf16 products themselves are exact; the
+// rounding error of a chain grows with its length (about 1e-6 for 4 MMAs,
+// 1e-4 for 384), so short chains keep the logits within a few 1e-6.
 //
 // Tile: 128 experts (M, router_w rows, K-major) x 64 tokens (N, xn rows,
 // K-major).  Split-K: a tile may cover only a range of k-blocks (small T
@@ -26,6 +28,7 @@
 namespace moe {
 
 constexpr int RT_BN = 64;           // tokens per tile
+constexpr int RT_CHAIN = 2;         // k-blocks accumulated in tensor memory per epilogue read
 constexpr int RT_STAGES = 6;
 constexpr int RT_NACC = 4;          // 64-column accumulators between MMA and epilogue
 constexpr int RT_EPI_WARPS = 8;
@@ -142,9 +145,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
             bool ok = true;
             RouterTile rt;
             for (int L = blockIdx.x; ok && router_tile(p, L, rt); L += gridDim.x) {
-                for (int kb = 0; kb < rt.nkb; ++kb, ++g) {
+                for (int kb = 0; kb < rt.nkb; ++kb) {
                     const uint32_t slot = g % RT_NACC;
-                    if (!mbar_wait(&tempty[slot], ((g / RT_NACC) & 1u) ^ 1u, abort_flag, RT_TIMEOUT_NS) ||
+                    const bool first = kb % RT_CHAIN == 0;
+                    const bool last = kb % RT_CHAIN == RT_CHAIN - 1 || kb == rt.nkb - 1;
+                    if ((first && !mbar_wait(&tempty[slot], ((g / RT_NACC) & 1u) ^ 1u, abort_flag,
+                                             RT_TIMEOUT_NS)) ||
                         !mbar_wait(&full[stage], phase, abort_flag, RT_TIMEOUT_NS)) {
                         ok = false;
                         break;
@@ -155,9 +161,13 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma_bf16(tmem_base + slot * 64, sdesc_sw128(a_addr + kk * 32, 16, 1024),
-                                    sdesc_sw128(b_addr + kk * 32, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+                                    sdesc_sw128(b_addr + kk * 32, 16, 1024), idesc,
+                                    (first && kk == 0) ? 0u : 1u);
                     tc_commit(&empty[stage]);
-                    tc_commit(&tfull[slot]);
+                    if (last) {
+                        tc_commit(&tfull[slot]);
+                        ++g;
+                    }
                     if (++stage == RT_STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -174,7 +184,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
             float hi[32], lo[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) { hi[c] = 0.f; lo[c] = 0.f; }
-            for (int kb = 0; kb < rt.nkb; ++kb, ++g) {
+            for (int kb = 0; kb < rt.nkb; kb += RT_CHAIN, ++g) {
                 const uint32_t slot = g % RT_NACC;
                 int good = 1;
                 if (lane == 0) good = mbar_wait(&tfull[slot], (g / RT_NACC) & 1u, abort_flag, RT_TIMEOUT_NS) ? 1 : 0;

@@ -57,3 +57,14 @@ def test_harness_catches_planted_errors(case):
     w2 = g["w"] * 1.001
     with pytest.raises(AssertionError):
         parity.check_routing_stage(dict(g, w=w2), host, c)
+
+
+def test_slot_order_may_swap_only_near_tied_experts():
+    b = np.array([[0.9, 0.5, 0.5 + 5e-7, 0.1]], np.float32)
+    oracle_sel = np.array([[0, 2, 1]])
+    set_diff, order_bad = parity.selection_diff(np.array([[0, 1, 2]]), oracle_sel, b)
+    assert not set_diff.any() and not order_bad.any()      # 1 and 2 are 5e-7 apart
+    set_diff, order_bad = parity.selection_diff(np.array([[1, 0, 2]]), oracle_sel, b)
+    assert not set_diff.any() and order_bad.all()          # 0.5 placed before 0.9
+    set_diff, _ = parity.selection_diff(np.array([[0, 1, 3]]), oracle_sel, b)
+    assert set_diff.all()
