@@ -167,6 +167,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_pair_kernel(const __gri
         // ------------------------------------------------ TMA producer (both CTAs)
         // One A load (16 KB) and one B load (8 or 16 KB) per k-block: the TMA
         // unit's cost grows with the number of copies, not only their bytes.
+        // A single lane waits and issues: it is usually ahead and really
+        // waits, and a whole warp polling the ring's barriers slows the
+        // barrier traffic the MMA warp and the copies depend on.
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
@@ -212,7 +215,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_pair_kernel(const __gri
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (leader only)
-        if (leader && lane == 0) {
+        // The whole warp runs the loop and the barrier waits (warp-uniform
+        // control flow and operands); one elected lane issues each MMA and
+        // commit.  Issuing from a single diverged lane measured slower.
+        if (leader) {
+            // Shared-memory descriptors are built once: the start address is the
+            // low field (address >> 4, below 2^14 for any shared address), and
+            // another ring stage or k-step of 16 is an add on it.
+            const uint64_t a_desc_mn = sdesc_sw128(smem_u32(sA), TC_BOX_BYTES, 1024);
+            const uint64_t a_desc_k = sdesc_sw128(smem_u32(sA), 16, 1024);
+            const uint64_t b_desc0 = sdesc_sw128(smem_u32(sB), 16, 1024);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -225,39 +237,55 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_pair_kernel(const __gri
                 const int n = (ti.rows + 15) & ~15;
                 const int a_mn = sg.grouped;
                 const uint32_t idesc = idesc_bf16_f32(2 * TC_BM, n, a_mn, 0);
-                if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, TC_TIMEOUT_NS)) {
-                    ok = false;
-                    break;
-                }
+                // one lane polls a barrier that is not ready; the warp takes its result
+                int got = 1;
+                if (lane == 0) got = mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, TC_TIMEOUT_NS);
+                ok = __shfl_sync(0xffffffffu, got, 0) != 0;
+                if (!ok) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PR_BN);
                 const int nkb = sg.K / TC_BK;
+                // MN-major A (grouped weights): 64-feature x 8-k atoms of 1 KB, the two
+                // 64-feature boxes 8 KB apart, a k-step of 16 moves two atoms (2 KB).
+                // K-major A and B: 8-row x 128-byte atoms, a k-step of 16 moves 32
+                // bytes inside the swizzled row.  The peer's halves sit at the same
+                // shared-memory offsets.
+                const uint64_t a_desc0 = a_mn ? a_desc_mn : a_desc_k;
+                const uint64_t a_kstep = a_mn ? (2048 >> 4) : (32 >> 4);
+                // Stage operands arrive by TMA and are read by the MMAs, both in the
+                // async proxy, ordered by the full barrier: no tcgen05 fence per stage.
+                // The try_wait of the next stage starts before this stage's MMAs, so
+                // its round trip overlaps their issue.
+                uint32_t ready = __all_sync(0xffffffffu, mbar_try_wait(&full[stage], phase)) ? 1u : 0u;
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, TC_TIMEOUT_NS)) {
-                        ok = false;
-                        break;
+                    if (!ready) {
+                        int got = 1;
+                        if (lane == 0) got = mbar_wait(&full[stage], phase, abort_flag, TC_TIMEOUT_NS);
+                        if (!__shfl_sync(0xffffffffu, got, 0)) {
+                            ok = false;
+                            break;
+                        }
                     }
-                    tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sA + stage * PR_A_BYTES);
-                    const uint32_t b_addr = smem_u32(sB + stage * PR_B_BYTES);
-#pragma unroll
-                    for (int kk = 0; kk < TC_BK / TC_UMMA_K; ++kk) {
-                        // descriptors as in tc_gemm_kernel; the peer's halves sit at
-                        // the same shared-memory offsets
-                        const uint64_t ad = a_mn ? sdesc_sw128(a_addr + kk * 2048, TC_BOX_BYTES, 1024)
-                                                 : sdesc_sw128(a_addr + kk * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(b_addr + kk * 32, 16, 1024);
-                        tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-                    }
-                    tc_commit_pair(&empty[stage], 0x3);
-                    if (++stage == PR_STAGES) { stage = 0; phase ^= 1u; }
+                    const int next = stage + 1 == PR_STAGES ? 0 : stage + 1;
+                    const uint32_t next_phase = stage + 1 == PR_STAGES ? phase ^ 1u : phase;
+                    const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage) * (PR_A_BYTES >> 4);
+                    const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage) * (PR_B_BYTES >> 4);
+                    ready = __all_sync(0xffffffffu,
+                                       mma4_pair_commit_trywait_warp(d_tmem, ad, bd, a_kstep, 32 >> 4, idesc,
+                                                                     kb > 0 ? 1u : 0u, &empty[stage], 0x3,
+                                                                     &full[next], next_phase) != 0u)
+                                ? 1u : 0u;
+                    stage = next;
+                    phase = next_phase;
                 }
                 if (!ok) break;
-                tc_commit_pair(&tfull[acc], 0x3);
+                tc_commit_pair_warp(&tfull[acc], 0x3);
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
-            tc_commit_pair(drain, 0x1);
-            mbar_wait(drain, 0, nullptr, ok ? TC_TIMEOUT_NS : TC_DRAIN_NS);
+            // wait until every MMA issued by this warp has completed
+            tc_commit_pair_warp(drain, 0x1);
+            if (lane == 0) mbar_wait(drain, 0, nullptr, ok ? TC_TIMEOUT_NS : TC_DRAIN_NS);
+            __syncwarp();
         }
     } else {
         // ------------------------------------------------ epilogue (warps 2-5, both CTAs)

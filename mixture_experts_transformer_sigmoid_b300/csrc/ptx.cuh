@@ -334,3 +334,72 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t mask) {
 
 }  // namespace moe
 
+
+namespace moe {
+// Four pair MMAs (K = 16 each, the descriptors advanced by a_step / b_step
+// per k-step) and a multicast commit of them to `commit_bar`, with a
+// try_wait on (next_bar, next_parity) started before the MMAs and read after
+// them: the barrier round trip overlaps the MMA issue instead of preceding
+// it.  Returns whether that phase had already completed.
+// Executed by a whole converged warp: every lane runs the try_wait, one
+// elected lane issues the MMAs and the commit (predicated, no branch).
+__device__ __forceinline__ uint32_t mma4_pair_commit_trywait_warp(uint32_t d_tmem, uint64_t ad, uint64_t bd,
+                                                                  uint64_t a_step, uint64_t b_step,
+                                                                  uint32_t idesc, uint32_t accumulate,
+                                                                  uint64_t* commit_bar, uint16_t mask,
+                                                                  uint64_t* next_bar, uint32_t next_parity) {
+    uint32_t ready;
+    asm volatile(
+        "{\n\t.reg .pred pe, pw, pa, pt;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+        "elect.sync _|pe, 0xffffffff;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 pw, [%10], %11;\n\t"
+        "setp.ne.b32 pa, %7, 0;\n\tsetp.eq.u32 pt, 1, 1;\n\t"
+        "add.s64 a1, %2, %4;\n\tadd.s64 a2, a1, %4;\n\tadd.s64 a3, a2, %4;\n\t"
+        "add.s64 b1, %3, %5;\n\tadd.s64 b2, b1, %5;\n\tadd.s64 b3, b2, %5;\n\t"
+        "@pe tcgen05.mma.cta_group::2.kind::f16 [%1], %2, %3, %6, pa;\n\t"
+        "@pe tcgen05.mma.cta_group::2.kind::f16 [%1], a1, b1, %6, pt;\n\t"
+        "@pe tcgen05.mma.cta_group::2.kind::f16 [%1], a2, b2, %6, pt;\n\t"
+        "@pe tcgen05.mma.cta_group::2.kind::f16 [%1], a3, b3, %6, pt;\n\t"
+        "@pe tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%8], %9;\n\t"
+        "selp.u32 %0, 1, 0, pw;\n\t}"
+        : "=r"(ready)
+        : "r"(d_tmem), "l"(ad), "l"(bd), "l"(a_step), "l"(b_step), "r"(idesc), "r"(accumulate),
+          "r"(smem_u32(commit_bar)), "h"(mask), "r"(smem_u32(next_bar)), "r"(next_parity)
+        : "memory");
+    return ready;
+}
+// A multicast pair commit issued by one elected lane of a converged warp.
+__device__ __forceinline__ void tc_commit_pair_warp(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "{\n\t.reg .pred pe;\n\telect.sync _|pe, 0xffffffff;\n\t"
+        "@pe tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t mma4_pair_commit_trywait(uint32_t d_tmem, uint64_t ad, uint64_t bd,
+                                                             uint64_t a_step, uint64_t b_step, uint32_t idesc,
+                                                             uint32_t accumulate, uint64_t* commit_bar,
+                                                             uint16_t mask, uint64_t* next_bar,
+                                                             uint32_t next_parity) {
+    uint32_t ready;
+    asm volatile(
+        "{\n\t.reg .pred pw, pa, pt;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 pw, [%10], %11;\n\t"
+        "setp.ne.b32 pa, %7, 0;\n\tsetp.eq.u32 pt, 1, 1;\n\t"
+        "add.s64 a1, %2, %4;\n\tadd.s64 a2, a1, %4;\n\tadd.s64 a3, a2, %4;\n\t"
+        "add.s64 b1, %3, %5;\n\tadd.s64 b2, b1, %5;\n\tadd.s64 b3, b2, %5;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], %2, %3, %6, pa;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], a1, b1, %6, pt;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], a2, b2, %6, pt;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%1], a3, b3, %6, pt;\n\t"
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%8], %9;\n\t"
+        "selp.u32 %0, 1, 0, pw;\n\t}"
+        : "=r"(ready)
+        : "r"(d_tmem), "l"(ad), "l"(bd), "l"(a_step), "l"(b_step), "r"(idesc), "r"(accumulate),
+          "r"(smem_u32(commit_bar)), "h"(mask), "r"(smem_u32(next_bar)), "r"(next_parity)
+        : "memory");
+    return ready;
+}
+}  // namespace moe
