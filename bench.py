@@ -36,10 +36,14 @@ from mixture_experts_transformer_sigmoid_b300 import workloads as wl  # noqa: E4
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 METRIC = "MoE sublayer tokens/s"
 
-# DRAM bytes per launch of the dominant kernel from the ncu capture summarised
-# in profiles/tc_gemm_glm5_slice.md (the slice scaled by 8 to the full
-# GLM-5 prefill launch).  Null once the kernel changes after that capture.
-TRAFFIC_PER_LAUNCH = {"glm5_prefill": {"gate_up_swiglu": 18.19e9, "down_weighted": 8.62e9}}
+# DRAM bytes (read + write) per launch of the grouped GEMMs from the ncu
+# capture summarised in profiles/tc_gemm_pair_glm5_slice.md: the GLM-5 slice
+# (32 experts, 1024 tokens) scaled by 8 to the full GLM-5 prefill launch
+# (routed experts and tokens grow 8x; the shared expert's 50 MB of weights do
+# not, so the figure overstates by at most 0.35 GB).  Null once the kernel
+# changes after that capture.
+TRAFFIC_PER_LAUNCH = {"glm5_prefill": {"gate_up_swiglu": 15.51e9, "down_weighted": 7.79e9}}
+GEMM_KERNEL = "tc_gemm_pair_kernel"
 
 
 def load_peaks():
@@ -179,15 +183,22 @@ def oracle_sample(w, host, n_tokens, seed=1):
 
 
 def cpu_baseline(w, host, target_s=15.0):
-    """The oracle timed on the host cores on a bounded sample (about
-    target_s seconds of CPU work), as tokens/s."""
+    """The oracle timed on the host cores on a bounded sample (at least
+    target_s seconds of CPU work after a warm-up call), as tokens/s."""
     from oracle import oracle as orc
-    t, _ = oracle_sample(w, host, 8, seed=2)            # calibration
-    n2 = int(min(w.T, max(8, round(8 * target_s / max(t, 1e-3)))))
-    t2, n2 = oracle_sample(w, host, n2, seed=3)
-    return {"value": round(n2 / t2, 3), "unit": "tokens/s", "cores": orc.num_threads(),
+    oracle_sample(w, host, 4, seed=2)                   # warm-up: thread pool, page-in
+    total_t, total_n, chunk, i = 0.0, 0, 32, 0
+    while total_t < target_s:
+        t, n = oracle_sample(w, host, chunk, seed=3 + i)
+        total_t += t
+        total_n += n
+        i += 1
+        if t < 2.0:
+            chunk = min(w.T, chunk * 2)
+    return {"value": round(total_n / total_t, 3), "unit": "tokens/s", "cores": orc.num_threads(),
             "kind": "oracle",
-            "sample": f"{n2} seeded tokens of the {w.name} workload ({t2:.1f} s, fp64 oracle)"}
+            "sample": f"{total_n} seeded tokens of the {w.name} workload in {i} batches "
+                      f"({total_t:.1f} s, fp64 oracle)"}
 
 
 # ------------------------------------------------------------ our arm
@@ -237,7 +248,7 @@ def run_ours(args, world, rank, local):
     dom_flops = gate_up_flops(w, T) if dominant == "gate_up_swiglu" else down_flops(w, T)
     dom_tf = dom_flops / (dom_ms / 1e3) / 1e12
     peak_tf = peaks["bf16_tflops"]
-    roofline = {"kernel": f"tc_gemm_kernel ({dominant})", "bound": "tensor",
+    roofline = {"kernel": f"{GEMM_KERNEL} ({dominant})", "bound": "tensor",
                 "achieved": round(dom_tf, 1), "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": round(dom_tf / peak_tf, 4),
                 "frac_of_sustained": round(dom_tf / peaks["bf16_tflops_sustained"], 4),
