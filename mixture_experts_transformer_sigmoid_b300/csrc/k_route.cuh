@@ -171,6 +171,69 @@ __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ ga
     }
 }
 
+// The same RMSNorm with one warp per token (no block barriers): each lane
+// keeps up to RMS_WARP_VECS 16-byte vectors of the row in registers, and the
+// compensated sum of squares is reduced with shuffles.  For d / V <=
+// 32 * RMS_WARP_VECS (d <= 6144 in bf16); rmsnorm_kernel covers longer rows.
+constexpr int RMS_WARP_VECS = 24;
+
+template <typename T>
+__global__ void rmsnorm_warp_kernel(const T* __restrict__ x, const T* __restrict__ gain,
+                                    T* __restrict__ xn, int n_tok, int d, float eps) {
+    constexpr int V = Elem<T>::V;
+    const int lane = threadIdx.x & 31;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= n_tok) return;
+    const int nvec = d / V;
+    const T* xr = x + static_cast<size_t>(t) * d;
+    int4 raw[RMS_WARP_VECS];
+#pragma unroll
+    for (int j = 0; j < RMS_WARP_VECS; ++j) {
+        const int v = lane + 32 * j;
+        if (v < nvec) raw[j] = __ldg(reinterpret_cast<const int4*>(xr) + v);
+    }
+    float hi = 0.f, lo = 0.f;
+#pragma unroll
+    for (int j = 0; j < RMS_WARP_VECS; ++j) {
+        if (lane + 32 * j >= nvec) continue;
+        const T* e = reinterpret_cast<const T*>(&raw[j]);
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const float f = Elem<T>::to_f(e[i]);
+            const float p = __fmul_rn(f, f);
+            const float pe = fmaf(f, f, -p);
+            float s, er;
+            two_sum_f(hi, p, s, er);
+            hi = s;
+            lo = __fadd_rn(lo, __fadd_rn(er, pe));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float oh = __shfl_xor_sync(0xffffffffu, hi, off);
+        const float ol = __shfl_xor_sync(0xffffffffu, lo, off);
+        float s, er;
+        two_sum_f(hi, oh, s, er);
+        hi = s;
+        lo = __fadd_rn(__fadd_rn(lo, ol), er);
+    }
+    const float ms = static_cast<float>((static_cast<double>(hi) + static_cast<double>(lo)) /
+                                        static_cast<double>(d));
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+#pragma unroll
+    for (int j = 0; j < RMS_WARP_VECS; ++j) {
+        const int v = lane + 32 * j;
+        if (v >= nvec) continue;
+        const T* e = reinterpret_cast<const T*>(&raw[j]);
+        float f[V], g[V];
+        load_vec<T>(gain + v * V, g);
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+            f[i] = __fmul_rn(g[i], Elem<T>::round_io(__fmul_rn(Elem<T>::to_f(e[i]), r)));
+        store_vec<T>(xn + static_cast<size_t>(t) * d + v * V, f);
+    }
+}
+
 // RMSNorm fused with the router logits on CUDA cores (fp32 accumulation):
 // one block per token; the normalised row stays in shared memory and each
 // warp takes experts e = warp, warp + nwarps, ... with 16-byte loads of the
@@ -445,6 +508,45 @@ __global__ void scatter_kernel(const int* __restrict__ idx, const float* __restr
         pos[static_cast<size_t>(t) * k + j] = row;
         row_tok[row] = t;
         row_w[row] = w[static_cast<size_t>(t) * k + j];
+    }
+}
+
+// xp[pos[t, j]] = xn[t] for every slot j: one warp per token, so each xn row
+// is read from memory once (a row-by-row gather re-reads it k times, and the
+// stream of writes evicts it from L2 in between).  16-byte vectors, eight in
+// flight per lane.  Rows outside [0, P) are skipped.
+template <typename T>
+__global__ void gather_tokens_kernel(const T* __restrict__ xn, const int* __restrict__ pos,
+                                     T* __restrict__ xp, int n_tok, int k, int d, int P) {
+    const int lane = threadIdx.x & 31;
+    const int nvec = d * static_cast<int>(sizeof(T)) / 16;
+    constexpr int U = 8;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tok;
+         t += (gridDim.x * blockDim.x) >> 5) {
+        const int4* src = reinterpret_cast<const int4*>(xn + static_cast<size_t>(t) * d);
+        int rows[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) rows[j] = j < k ? pos[static_cast<size_t>(t) * k + j] : -1;
+        for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+            int4 r[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v < nvec) r[u] = __ldg(src + v);
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (j >= k) break;
+                const int row = rows[j];
+                if (row < 0 || row >= P) continue;
+                int4* dst = reinterpret_cast<int4*>(xp + static_cast<size_t>(row) * d);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int v = v0 + u * 32 + lane;
+                    if (v < nvec) dst[v] = r[u];
+                }
+            }
+        }
     }
 }
 

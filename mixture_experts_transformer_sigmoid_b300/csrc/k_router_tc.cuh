@@ -4,7 +4,7 @@
 // A tensor-core accumulation chained over the whole hidden size (hundreds of
 // MMAs into one fp32 accumulator) carries a rounding error that grows with
 // the chain and can exceed the top-k margins the routing must resolve
-// (biased-score gaps down to 1e-5).  So every RT_CHAIN k-blocks of 64 (8
+// (biased-score gaps down to 1e-5).  So every RT_CHAIN k-blocks of 64 (16
 // MMAs) start a fresh accumulator in tensor memory, and the epilogue warps
 // add the chain results into a compensated (hi, lo) fp32 pair with an
 // error-free two-sum.  The bf16 x bf16 products themselves are exact; the
@@ -28,7 +28,7 @@
 namespace moe {
 
 constexpr int RT_BN = 64;           // tokens per tile
-constexpr int RT_CHAIN = 2;         // k-blocks accumulated in tensor memory per epilogue read
+constexpr int RT_CHAIN = 4;         // k-blocks accumulated in tensor memory per epilogue read
 constexpr int RT_STAGES = 6;
 constexpr int RT_NACC = 4;          // 64-column accumulators between MMA and epilogue
 constexpr int RT_EPI_WARPS = 8;

@@ -247,8 +247,20 @@ template <int EPL>
 void launch_topk_e(const float2* part, const float* bias, int T, int E, int k, float scale,
                    float* logits, int* idx, float* w, int* chunk_cnt, cudaStream_t st) {
     const int n_chunks = (T + CHUNK_TOKENS - 1) / CHUNK_TOKENS;
-    topk_kernel<EPL><<<n_chunks, 512, E * sizeof(int), st>>>(part, bias, T, E, k, scale, logits,
-                                                             idx, w, chunk_cnt);
+    // one block per 128-token chunk (its histogram): the chunk count is small next to
+    // the SM count, so each block takes as many warps as its registers allow (up to 32)
+    static int threads[64] = {};  // per device, found before the first launch
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) dev = 0;
+    if (threads[dev] == 0) {
+        cudaFuncAttributes fa;
+        int tmax = 512;
+        if (cudaFuncGetAttributes(&fa, topk_kernel<EPL>) == cudaSuccess)
+            tmax = std::min(1024, fa.maxThreadsPerBlock) / 32 * 32;
+        threads[dev] = std::max(32, tmax);
+    }
+    topk_kernel<EPL><<<n_chunks, threads[dev], E * sizeof(int), st>>>(part, bias, T, E, k, scale, logits,
+                                                                      idx, w, chunk_cnt);
 }
 
 void launch_topk(const float2* part, const float* bias, int T, int E, int k, float scale,
@@ -322,7 +334,13 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     // A+B: RMSNorm and router logits
     mark(h, 0, st);
     if (h->tc) {
-        rmsnorm_kernel<T><<<Tn, 256, 0, st>>>(x, static_cast<const T*>(a.norm_w), xn, d, c.eps);
+        // a warp per token once there are enough tokens to fill the SMs; small
+        // batches (decode) keep a whole block on each token
+        if (d / Elem<T>::V <= 32 * RMS_WARP_VECS && Tn >= 8 * h->num_sms)
+            rmsnorm_warp_kernel<T><<<(Tn + 7) / 8, 256, 0, st>>>(x, static_cast<const T*>(a.norm_w), xn, Tn,
+                                                                 d, c.eps);
+        else
+            rmsnorm_kernel<T><<<Tn, 256, 0, st>>>(x, static_cast<const T*>(a.norm_w), xn, d, c.eps);
         mark(h, 1, st);
         const int n_router = launch_router_tc(h, a.router_w, xn, Tn, st);
         if (n_router == 0) return MOE_ERR_CUDA;
@@ -345,8 +363,12 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     scatter_kernel<<<n_chunks, CHUNK_TOKENS, E * (CHUNK_TOKENS / 32) * sizeof(uint32_t), st>>>(
         h->topk_idx, h->topk_w, Tn, E, k, h->chunk_base, h->pos, h->row_tok, h->row_w);
     mark(h, 5, st);
-    gather_rows_kernel<T><<<std::min(4 * h->num_sms, (P + 7) / 8), 256, 0, st>>>(
-        xn, h->row_tok, static_cast<T*>(h->xp), P, d, Tn);
+    if (Tn >= 8 * h->num_sms)   // a warp per token: each xn row read once
+        gather_tokens_kernel<T><<<std::min(8 * h->num_sms, (Tn + 7) / 8), 256, 0, st>>>(
+            xn, h->pos, static_cast<T*>(h->xp), Tn, k, d, P);
+    else                        // few tokens: a warp per row spreads the copy over more SMs
+        gather_rows_kernel<T><<<std::min(4 * h->num_sms, (P + 7) / 8), 256, 0, st>>>(
+            xn, h->row_tok, static_cast<T*>(h->xp), P, d, Tn);
     h->launches += 4;
     mark(h, 6, st);
 

@@ -89,6 +89,11 @@ WORKLOADS: Dict[str, Workload] = {
     "glm5_slice": Workload("glm5_slice", T=1024, d=6144, E=32, I=2048,
                            Is=2048, k=8, routed_scale=2.5, dtype="bf16",
                            description="T1024 d6144 E32 I2048 k8 bf16"),
+    # GLM-5 routing shapes (tokens, hidden, experts, top-k) with narrow
+    # experts (0.6 GB of weights): the profiling case of the routing kernels.
+    "glm5_routing": Workload("glm5_routing", T=8192, d=6144, E=256, I=64,
+                             Is=64, k=8, routed_scale=2.5, dtype="bf16",
+                             description="T8192 d6144 E256 I64 k8 bf16"),
 }
 
 
