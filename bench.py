@@ -6,7 +6,9 @@
 
 One step is one forward pass of the whole sublayer (RMSNorm, sigmoid router
 and top-k, permutation, routed SwiGLU experts, shared expert, combine and
-residual) over one batch of synthetic tokens already resident in HBM.  With
+residual) over one batch of synthetic tokens already resident in HBM,
+launched as the replay of a CUDA graph that captured one moe_forward call.
+Per-stage times come from a second, directly launched pass of the same steps.  With
 N > 1 (launched by torch.distributed.run) every rank holds a full replica of
 the weights and runs its own batch: no collective is on the data path, so
 scaling is weak and the value is the tokens of all ranks per second.
@@ -221,8 +223,14 @@ def run_ours(args, world, rank, local):
     for _ in range(args.warmup):
         layer.forward(inp["x"], inp, w.k, w.routed_scale, out=out)
     assert layer.sync_status() == B.MOE_OK
-    layer.set_profiling(True)
-    layer.read_stats()
+    # The step is one moe_forward captured in a CUDA graph and replayed, as a
+    # serving loop would launch it (the forward allocates nothing and never
+    # synchronises).
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(inp["x"], inp, w.k, w.routed_scale, out=out)
+    graph.replay()
+    torch.cuda.synchronize()
 
     barrier(world)
     torch.cuda.synchronize()
@@ -230,11 +238,19 @@ def run_ours(args, world, rank, local):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        layer.forward(inp["x"], inp, w.k, w.routed_scale, out=out)
+        graph.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     ms = e0.elapsed_time(e1) / args.steps
+    assert layer.sync_status() == B.MOE_OK
+    del graph
+    # Per-stage times (CUDA events on the launching stream) and the kernel count
+    # per forward, from the same number of steps launched directly.
+    layer.set_profiling(True)
+    layer.read_stats()
+    for _ in range(args.steps):
+        layer.forward(inp["x"], inp, w.k, w.routed_scale, out=out)
     st = layer.read_stats()
     layer.set_profiling(False)
     assert layer.sync_status() == B.MOE_OK
@@ -271,7 +287,8 @@ def run_ours(args, world, rank, local):
         "tensor_frac_whole_step": round(whole_tf / peak_tf, 4),
         "roofline": roofline,
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
-        "gpu_launches": st["launches"],
+        "gpu_launches": st["launches"],   # kernels of the timed steps (graph replays launch the same)
+        "launch": "CUDA graph replay of one moe_forward per step",
     }
 
     # ---- decode: GLM-5 shapes, T = 64, skewed routing, L2 flushed per step
@@ -318,20 +335,35 @@ def run_decode(args, inp3, local, peaks, peak_src, world):
     assert layer.sync_status() == B.MOE_OK
     _, _, counts = layer.routing()
     n_active = int((counts > 0).sum().item())
-    layer.set_profiling(True)
-    layer.read_stats()
     n_iter = max(50, args.steps * 4)
+    # Step time: the forward captured once in a CUDA graph and replayed (a decode
+    # step's kernels are short enough that host launch latency would otherwise
+    # show up between them); L2 flushed before every step, outside the events.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(dinp["x"], dinp, w.k, w.routed_scale, out=out)
+    torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n_iter)]
     for a, b in evs:
         flush.zero_()                       # evict the previous step's weights from L2
         a.record(stream)
-        layer.forward(dinp["x"], dinp, w.k, w.routed_scale, out=out)
+        graph.replay()
         b.record(stream)
     torch.cuda.synchronize()
     times = [a.elapsed_time(b) for a, b in evs]
+    assert layer.sync_status() == B.MOE_OK
+    # Stage times (for the kernel roofline): the same steps launched directly with
+    # per-stage CUDA events.
+    layer.set_profiling(True)
+    layer.read_stats()
+    for _ in range(n_iter):
+        flush.zero_()
+        layer.forward(dinp["x"], dinp, w.k, w.routed_scale, out=out)
+    torch.cuda.synchronize()
     st = layer.read_stats()
     layer.set_profiling(False)
+    del graph
     layer.close()
     ms = statistics.median(times)
     nbytes = decode_bytes(w, w.T, n_active)
@@ -346,6 +378,7 @@ def run_decode(args, inp3, local, peaks, peak_src, world):
             "tokens_per_s": round(world * w.T / (ms / 1e3), 1),
             "bytes_per_step": nbytes, "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
             "l2": "256 MB buffer written between steps (outside the timed events)",
+            "launch": "CUDA graph replay of one moe_forward",
             "roofline": {"kernel": "tc_gemm_kernel (gate_up_swiglu)", "bound": "hbm",
                          "achieved": round(gu_gbs, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(gu_gbs / hbm, 4), "peak_source": f"{peak_src} HBM copy",

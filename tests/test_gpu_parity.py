@@ -175,3 +175,28 @@ def test_air_prefill_workload():
 @pytest.mark.parametrize("name", ["glm5_decode", "glm5_prefill"])
 def test_glm5_workloads(name):
     workload_check(name, dev_gen=True)
+
+
+@pytest.mark.parametrize("name", ["ragged_bf16", "skewed_bf16"])   # CTA-pair / single-CTA GEMM paths
+def test_forward_replayed_from_cuda_graph_matches_direct_call(name):
+    """moe_forward allocates nothing and never synchronises, so a serving loop
+    can capture it in a CUDA graph; the replay must give the same bytes."""
+    from mixture_experts_transformer_sigmoid_b300 import binding as B
+    w = SMALL[name]
+    inp = device_inputs(wl.make_inputs(w))
+    layer = B.MoeSublayer(max_tokens=w.T, hidden=w.d, n_experts=w.E, inter=w.I,
+                          shared_inter=w.Is, max_top_k=w.k, dtype=w.dtype)
+    try:
+        direct = layer.forward(inp["x"], inp, w.k, w.routed_scale).clone()
+        out = torch.empty_like(direct)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            layer.forward(inp["x"], inp, w.k, w.routed_scale, out=out)
+        graph.replay()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert layer.sync_status() == B.MOE_OK
+        assert torch.equal(out, direct)
+        del graph
+    finally:
+        layer.close()
