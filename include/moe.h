@@ -117,6 +117,27 @@ MOE_API moe_status moe_forward_host(moe_handle* h, int32_t T, const void* x_host
                             const void* shared_down, int32_t top_k, float routed_scale,
                             void* out_host, void* stream);
 
+/* Pipelined form of moe_forward_host for a stream of batches: queues the
+ * H2D copy of x (on an internal copy stream), the forward (on `stream`) and
+ * the D2H copy of the result (on a second copy stream) and returns without
+ * waiting, so one batch's copies overlap the neighbouring batches' forwards.
+ * Two staging slots alternate between calls; events keep each slot from being
+ * overwritten before its previous forward and copy-out are done.  The caller
+ * keeps x_host and out_host valid and unread until moe_forward_host_wait
+ * returns; x_host/out_host should be pinned (pageable memory works but does
+ * not overlap).  Same argument checks as moe_forward_host.  Not for
+ * concurrent calls on one handle from several threads. */
+MOE_API moe_status moe_forward_host_async(moe_handle* h, int32_t T, const void* x_host, const void* norm_w,
+                                  const void* router_w, const float* corr_bias, const void* gate_up,
+                                  const void* down, const void* shared_gate, const void* shared_up,
+                                  const void* shared_down, int32_t top_k, float routed_scale,
+                                  void* out_host, void* stream);
+
+/* Waits for every moe_forward_host_async call queued on this handle (their
+ * results are then in the callers' out_host buffers) and reports the device
+ * error flag like moe_sync_status. */
+MOE_API moe_status moe_forward_host_wait(moe_handle* h);
+
 /* Routing of the last forward on this handle, copied (device to device, on
  * `stream`) into caller buffers; any pointer may be NULL:
  *   idx [T, top_k] int32 expert ids in slot order, w [T, top_k] fp32 weights,

@@ -21,7 +21,8 @@ DTYPE_FP32, DTYPE_BF16 = 0, 1
 T_XN, T_LOGITS, T_OFFSETS, T_POS, T_ROW_TOK, T_H, T_SHARED = range(7)
 
 # Functions the header declares (kept in sync by the ABI test).
-EXPORTS = ("moe_init", "moe_forward", "moe_forward_host", "moe_get_routing",
+EXPORTS = ("moe_init", "moe_forward", "moe_forward_host", "moe_forward_host_async",
+           "moe_forward_host_wait", "moe_get_routing",
            "moe_get_intermediate", "moe_sync_status", "moe_set_profiling", "moe_read_stats",
            "moe_destroy", "moe_route_static", "moe_status_string")
 STAGES = ("rmsnorm", "router", "topk", "scan", "scatter", "gather", "gate_up_swiglu",
@@ -64,6 +65,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     fwd = [P, I32, P, P, P, P, P, P, P, P, P, I32, F32, P, P]
     lib.moe_forward.argtypes = fwd
     lib.moe_forward_host.argtypes = fwd
+    lib.moe_forward_host_async.argtypes = fwd
+    lib.moe_forward_host_wait.argtypes = [P]
     lib.moe_get_routing.argtypes = [P, P, P, P, P]
     lib.moe_get_intermediate.argtypes = [P, ctypes.c_int, P, ctypes.c_size_t, P]
     lib.moe_sync_status.argtypes = [P, P]
@@ -152,6 +155,22 @@ class MoeSublayer:
             top_k, routed_scale, _ptr(out_host), self._stream(stream)), "moe_forward_host")
         self.last_T, self.last_k = T, top_k
         return out_host
+
+    def forward_host_async(self, x_host, w: dict, top_k: int, routed_scale: float, out_host,
+                           stream=None):
+        """Queues one host-buffer forward without waiting (pipelined copies);
+        out_host is filled once forward_host_wait returns."""
+        T = x_host.shape[0]
+        _check(self.lib.moe_forward_host_async(
+            self.handle, T, _ptr(x_host), _ptr(w["norm_w"]), _ptr(w["router_w"]),
+            _ptr(w["corr_bias"]), _ptr(w["gate_up"]), _ptr(w["down"]),
+            _ptr(w.get("shared_gate")), _ptr(w.get("shared_up")), _ptr(w.get("shared_down")),
+            top_k, routed_scale, _ptr(out_host), self._stream(stream)), "moe_forward_host_async")
+        self.last_T, self.last_k = T, top_k
+        return out_host
+
+    def forward_host_wait(self):
+        _check(self.lib.moe_forward_host_wait(self.handle), "moe_forward_host_wait")
 
     def routing(self, stream=None):
         T, k, E = self.last_T, self.last_k, self.cfg.n_experts

@@ -57,6 +57,13 @@ struct moe_handle {
     void* sh = nullptr;
     void* x_stage = nullptr;
     void* out_stage = nullptr;
+    // pipelined host I/O (moe_forward_host_async): a second staging slot, copy
+    // streams and the events that order each slot's reuse
+    void* x_stage2 = nullptr;
+    void* out_stage2 = nullptr;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t ev_in[2] = {}, ev_done[2] = {}, ev_out[2] = {};
+    int async_slot = 0;
     int* err = nullptr;
     int last_T = 0;
     int last_k = 0;
@@ -144,7 +151,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 void free_ws(moe_handle* h) {
     void* ptrs[] = {h->xn, h->logits, h->part, h->topk_idx, h->topk_w, h->chunk_cnt, h->chunk_base,
                     h->counts, h->offsets, h->pos, h->row_tok, h->row_w, h->xp, h->h, h->yp,
-                    h->hs, h->sh, h->x_stage, h->out_stage, h->err};
+                    h->hs, h->sh, h->x_stage, h->out_stage, h->x_stage2, h->out_stage2, h->err};
     for (void* p : ptrs)
         if (p) cudaFree(p);
 }
@@ -675,6 +682,8 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out) {
     alloc(&h->sh, T * d * es);
     alloc(&h->x_stage, T * d * es);
     alloc(&h->out_stage, T * d * es);
+    alloc(&h->x_stage2, T * d * es);
+    alloc(&h->out_stage2, T * d * es);
     alloc(&h->err, 4);
     if (ok && cudaMemset(h->err, 0, 4) != cudaSuccess) ok = false;
     if (!ok) {
@@ -682,6 +691,17 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out) {
         free_ws(h);
         delete h;
         return MOE_ERR_OOM;
+    }
+    bool ev_ok = cudaStreamCreateWithFlags(&h->h2d, cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaStreamCreateWithFlags(&h->d2h, cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; i < 2 && ev_ok; ++i)
+        ev_ok = cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+                cudaEventCreateWithFlags(&h->ev_done[i], cudaEventDisableTiming) == cudaSuccess &&
+                cudaEventCreateWithFlags(&h->ev_out[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ev_ok) {
+        cudaGetLastError();
+        moe_destroy(h);
+        return MOE_ERR_CUDA;
     }
     *out = h;
     return MOE_OK;
@@ -720,6 +740,52 @@ moe_status moe_forward_host(moe_handle* h, int32_t T, const void* x_host, const 
     if (bytes && cudaMemcpyAsync(out_host, h->out_stage, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     return moe_sync_status(h, stream);
+}
+
+moe_status moe_forward_host_async(moe_handle* h, int32_t T, const void* x_host, const void* norm_w,
+                                  const void* router_w, const float* corr_bias, const void* gate_up,
+                                  const void* down, const void* shared_gate, const void* shared_up,
+                                  const void* shared_down, int32_t top_k, float routed_scale,
+                                  void* out_host, void* stream) {
+    FwdArgs a{T, x_host, norm_w, router_w, corr_bias, gate_up, down, shared_gate, shared_up,
+              shared_down, top_k, routed_scale, out_host};
+    moe_status s = validate_forward(h, a, true);
+    if (s != MOE_OK) return s;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int slot = h->async_slot;
+    void* xs = slot == 0 ? h->x_stage : h->x_stage2;
+    void* os = slot == 0 ? h->out_stage : h->out_stage2;
+    const size_t bytes = static_cast<size_t>(T) * h->cfg.hidden * h->es;
+    // H2D once the slot's previous forward has read its input
+    if (cudaStreamWaitEvent(h->h2d, h->ev_done[slot], 0) != cudaSuccess ||
+        (bytes && cudaMemcpyAsync(xs, x_host, bytes, cudaMemcpyHostToDevice, h->h2d) != cudaSuccess) ||
+        cudaEventRecord(h->ev_in[slot], h->h2d) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    // the forward once its input is in and the slot's previous output copied out
+    if (cudaStreamWaitEvent(st, h->ev_in[slot], 0) != cudaSuccess ||
+        cudaStreamWaitEvent(st, h->ev_out[slot], 0) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    a.x = xs;
+    a.out = os;
+    s = forward_impl(h, a, st);
+    if (s != MOE_OK) return s;
+    if (cudaEventRecord(h->ev_done[slot], st) != cudaSuccess) return MOE_ERR_CUDA;
+    // D2H once the forward is done
+    if (cudaStreamWaitEvent(h->d2h, h->ev_done[slot], 0) != cudaSuccess ||
+        (bytes && cudaMemcpyAsync(out_host, os, bytes, cudaMemcpyDeviceToHost, h->d2h) != cudaSuccess) ||
+        cudaEventRecord(h->ev_out[slot], h->d2h) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    h->async_slot = slot ^ 1;
+    return MOE_OK;
+}
+
+moe_status moe_forward_host_wait(moe_handle* h) {
+    if (!h) return MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(h->h2d) != cudaSuccess || cudaStreamSynchronize(h->d2h) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return moe_sync_status(h, h->d2h);
 }
 
 moe_status moe_get_routing(moe_handle* h, int32_t* idx, float* w, int32_t* counts, void* stream) {
@@ -815,6 +881,13 @@ moe_status moe_destroy(moe_handle* h) {
     cudaSetDevice(h->cfg.device);
     cudaDeviceSynchronize();
     for (auto& e : h->ev) cudaEventDestroy(e);
+    for (int i = 0; i < 2; ++i) {
+        if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
+        if (h->ev_done[i]) cudaEventDestroy(h->ev_done[i]);
+        if (h->ev_out[i]) cudaEventDestroy(h->ev_out[i]);
+    }
+    if (h->h2d) cudaStreamDestroy(h->h2d);
+    if (h->d2h) cudaStreamDestroy(h->d2h);
     free_ws(h);
     delete h;
     return MOE_OK;
