@@ -126,3 +126,9 @@ def test_binding_fails_loudly_without_library(tmp_path):
 def test_route_static_host_checks(lib, T, E, k, status):
     nulls = [None] * 9
     assert lib.moe_route_static(T, E, k, 1.0, *nulls, None) == status
+
+
+def test_host_io_entry_points_reject_a_null_handle(lib):
+    nulls = [None] * 11
+    assert lib.moe_forward_host_async(None, 4, *nulls[:9], 2, 1.0, None, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_forward_host_wait(None) == B.MOE_ERR_INVALID_ARG

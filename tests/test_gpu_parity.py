@@ -41,6 +41,9 @@ SMALL = {
     # feature tiles in both GEMMs and a shared expert narrower than one pair tile
     "pair_odd_sizes_bf16": W("pair_odd_sizes_bf16", T=1000, d=320, E=8, I=192, Is=64, k=3,
                              routed_scale=2.5, dtype="bf16"),
+    # one routed expert, top-1: the sublayer reduces to two dense SwiGLU MLPs
+    "one_expert_bf16": W("one_expert_bf16", T=256, d=256, E=1, I=128, Is=64, k=1,
+                         routed_scale=1.0, dtype="bf16"),
     "tiny_fp32": wl.WORKLOADS["tiny_fp32"],
     "ragged_fp32": W("ragged_fp32", T=77, d=128, E=6, I=64, Is=32, k=2, routed_scale=1.0,
                      dtype="fp32", bias_range=0.1),
