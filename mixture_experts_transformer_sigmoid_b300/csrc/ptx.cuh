@@ -70,23 +70,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0,
-                                            int c1, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0,
-                                            int c1, int c2, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
-        "l"(policy)
-        : "memory");
-}
 __device__ __forceinline__ void tma_load_2d_nohint(void* dst, const CUtensorMap* m, uint64_t* bar,
                                                    int c0, int c1) {
     asm volatile(
@@ -102,17 +85,6 @@ __device__ __forceinline__ void tma_load_3d_nohint(void* dst, const CUtensorMap*
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
-}
-// L2 eviction policies for the cache_hint operand.
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
 }
 
 // ----------------------------------------------------------------- tcgen05
@@ -277,14 +249,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
         "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1)
         : "memory");
 }
-__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster,
-                                                 int c0, int c1, int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
 
 __device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster,
                                                  int c0, int c1, int c2, int c3) {
@@ -309,40 +273,19 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                  : "memory");
 }
-// D (+)= A * B over the pair: A rows 0-127 come from the issuing CTA's
-// shared memory and rows 128-255 from the peer's (same address); B's first
-// N/2 rows from the issuing CTA and the rest from the peer; each CTA's
-// tensor memory receives its own 128 rows of D, all N columns.
-__device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive on the mbarrier at this offset in every CTA of `mask` once the
-// pair MMAs issued so far have completed.
-__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
 
-}  // namespace moe
-
-
-namespace moe {
-// Four pair MMAs (K = 16 each, the descriptors advanced by a_step / b_step
-// per k-step) and a multicast commit of them to `commit_bar`, with a
-// try_wait on (next_bar, next_parity) started before the MMAs and read after
-// them: the barrier round trip overlaps the MMA issue instead of preceding
-// it.  Returns whether that phase had already completed.
-// Executed by a whole converged warp: every lane runs the try_wait, one
-// elected lane issues the MMAs and the commit (predicated, no branch).
+// Four pair MMAs D (+)= A * B (tcgen05.mma.cta_group::2, M = 256, K = 16
+// each; the descriptors advanced by a_step / b_step per k-step): A rows
+// 0-127 come from the issuing CTA's shared memory and rows 128-255 from the
+// peer's (same address); B's first N/2 rows from the issuing CTA and the
+// rest from the peer; each CTA's tensor memory receives its own 128 rows of
+// D, all N columns.  Then a commit of them to `commit_bar` in every CTA of
+// `mask`, and a try_wait on (next_bar, next_parity) started before the MMAs
+// and read after them, so the barrier round trip overlaps the MMA issue
+// instead of preceding it.  Returns whether that phase had already
+// completed.  Executed by a whole converged warp: every lane runs the
+// try_wait, one elected lane issues the MMAs and the commit (predicated, no
+// branch).
 __device__ __forceinline__ uint32_t mma4_pair_commit_trywait_warp(uint32_t d_tmem, uint64_t ad, uint64_t bd,
                                                                   uint64_t a_step, uint64_t b_step,
                                                                   uint32_t idesc, uint32_t accumulate,
@@ -378,28 +321,4 @@ __device__ __forceinline__ void tc_commit_pair_warp(uint64_t* bar, uint16_t mask
         : "memory");
 }
 
-__device__ __forceinline__ uint32_t mma4_pair_commit_trywait(uint32_t d_tmem, uint64_t ad, uint64_t bd,
-                                                             uint64_t a_step, uint64_t b_step, uint32_t idesc,
-                                                             uint32_t accumulate, uint64_t* commit_bar,
-                                                             uint16_t mask, uint64_t* next_bar,
-                                                             uint32_t next_parity) {
-    uint32_t ready;
-    asm volatile(
-        "{\n\t.reg .pred pw, pa, pt;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 pw, [%10], %11;\n\t"
-        "setp.ne.b32 pa, %7, 0;\n\tsetp.eq.u32 pt, 1, 1;\n\t"
-        "add.s64 a1, %2, %4;\n\tadd.s64 a2, a1, %4;\n\tadd.s64 a3, a2, %4;\n\t"
-        "add.s64 b1, %3, %5;\n\tadd.s64 b2, b1, %5;\n\tadd.s64 b3, b2, %5;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], %2, %3, %6, pa;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], a1, b1, %6, pt;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], a2, b2, %6, pt;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%1], a3, b3, %6, pt;\n\t"
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%8], %9;\n\t"
-        "selp.u32 %0, 1, 0, pw;\n\t}"
-        : "=r"(ready)
-        : "r"(d_tmem), "l"(ad), "l"(bd), "l"(a_step), "l"(b_step), "r"(idesc), "r"(accumulate),
-          "r"(smem_u32(commit_bar)), "h"(mask), "r"(smem_u32(next_bar)), "r"(next_parity)
-        : "memory");
-    return ready;
-}
 }  // namespace moe
