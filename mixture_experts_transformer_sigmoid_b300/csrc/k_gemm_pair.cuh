@@ -11,14 +11,15 @@
 // is 6 deep instead of 4, and each token tile is read from L2 by half as
 // many CTAs.
 //
-// Roles.  Warp 0 of each CTA loads its own A and B halves; both CTAs'
-// copies count on the leader's (rank 0) `full` barrier, so the leader's
-// single MMA thread sees one barrier per stage.  The leader issues every
-// MMA and commits to the `empty` and `tfull` barriers of both CTAs at once
-// (multicast).  Warps 2-5 of each CTA drain its own tensor memory; all
-// eight epilogue warps arrive on the leader's `tempty` barrier.  Every wait
-// is bounded; a CTA that gives up sets the device error flag, and both CTAs
-// still meet at the final cluster barrier before tensor memory is freed.
+// Roles.  Lane 0 of warp 0 of each CTA loads its own A and B halves (one
+// TMA copy each per k-block); both CTAs' copies count on the leader's (rank
+// 0) `full` barrier, so the leader's MMA warp sees one barrier per stage.
+// The leader's warp 1 issues every MMA from one elected lane and commits to
+// the `empty` and `tfull` barriers of both CTAs at once (multicast).  Warps
+// 2-5 of each CTA drain its own tensor memory; all eight epilogue warps
+// arrive on the leader's `tempty` barrier.  Every wait is bounded; a CTA
+// that gives up sets the device error flag, and both CTAs still meet at the
+// final cluster barrier before tensor memory is freed.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -47,8 +48,6 @@ struct PrSmem {
     static constexpr uint32_t TOTAL = 1024 + RING + BARS + MISC + PREFIX + XBUF;
 };
 
-// Position of a CTA's producer in its sequence of (tile, k-block) loads, with
-// the coordinates of the CTA's half of the tile.
 // How a CTA's 128 A rows arrive, one k-block at a time (16 KB either way).
 enum PairAKind {
     PA_TWO_2D = 0,      // two 64-row boxes of K-major maps: a0 at row f0, a1 at row f0 + a_foff1
@@ -57,6 +56,8 @@ enum PairAKind {
     PA_CHUNKS_4D = 3    // grouped down: 4-D map {feature, k, 64-feature chunk, expert}, chunks f0/64 and f0/64 + 1
 };
 
+// Position of a CTA's producer in its sequence of (tile, k-block) loads, with
+// the coordinates of the CTA's half of the tile.
 struct PairCursor {
     int L, kb, nkb;
     int f0;      // first feature of this CTA's A rows
