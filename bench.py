@@ -160,9 +160,26 @@ def max_over_ranks(v: float, world: int) -> float:
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_throughput(world: int, tokens_per_rank: int, ms_local: float):
+    """Whole-job tokens/s of `world` replicas that each process
+    tokens_per_rank tokens per step: the slowest rank's step time bounds the
+    job.  Returns (that time in ms, tokens/s)."""
+    ms_max = max_over_ranks(ms_local, world)
+    return ms_max, world * tokens_per_rank / (ms_max / 1e3)
+
+
+def replica_inputs(w, rank: int, device: str):
+    """Rank 0's inputs; other ranks keep the same weights and draw their own batch."""
+    inp = wl.make_inputs(w, seed=0, device=device)
+    if rank > 0:
+        inp["x"] = wl.make_inputs(w, seed=rank, device=device, weights_from=inp)["x"]
+    return inp
 
 
 def gpu_index(local):
@@ -208,9 +225,7 @@ def run_ours(args, world, rank, local):
     from mixture_experts_transformer_sigmoid_b300 import binding as B
     peaks, peak_src = load_peaks()
     w = wl.WORKLOADS[args.workload]
-    inp = wl.make_inputs(w, seed=0, device="cuda")
-    if rank > 0:   # each replica its own batch, the same weights
-        inp["x"] = wl.make_inputs(w, seed=rank, device="cuda", weights_from=inp)["x"]
+    inp = replica_inputs(w, rank, "cuda")   # each replica its own batch, the same weights
     torch.cuda.synchronize()
     T = w.T
     layer = B.MoeSublayer(max_tokens=T, hidden=w.d, n_experts=w.E, inter=w.I, shared_inter=w.Is,
@@ -243,6 +258,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     ms = e0.elapsed_time(e1) / args.steps
+    ms_max, value = replica_throughput(world, T, ms)
     assert layer.sync_status() == B.MOE_OK
     del graph
     # Per-stage times (CUDA events on the launching stream) and the kernel count
@@ -254,8 +270,6 @@ def run_ours(args, world, rank, local):
     st = layer.read_stats()
     layer.set_profiling(False)
     assert layer.sync_status() == B.MOE_OK
-    ms_max = max_over_ranks(ms, world)
-    value = world * T / (ms_max / 1e3)
 
     stage_ms = {k: v / args.steps for k, v in st["stage_ms"].items()}
     gu_ms, dn_ms = stage_ms["gate_up_swiglu"], stage_ms["down_weighted"]
