@@ -41,6 +41,10 @@ SMALL = {
     # feature tiles in both GEMMs and a shared expert narrower than one pair tile
     "pair_odd_sizes_bf16": W("pair_odd_sizes_bf16", T=1000, d=320, E=8, I=192, Is=64, k=3,
                              routed_scale=2.5, dtype="bf16"),
+    # every token routed to one hot expert (bias +5): one expert with 1500 rows, six
+    # token tiles on the CTA-pair path, the other slot spread over the rest
+    "all_hot_expert_bf16": W("all_hot_expert_bf16", T=1500, d=256, E=16, I=128, Is=64, k=2,
+                             routed_scale=2.5, dtype="bf16", n_hot=1, hot_bias=5.0),
     # one routed expert, top-1: the sublayer reduces to two dense SwiGLU MLPs
     "one_expert_bf16": W("one_expert_bf16", T=256, d=256, E=1, I=128, Is=64, k=1,
                          routed_scale=1.0, dtype="bf16"),
@@ -225,3 +229,23 @@ def test_pipelined_host_forward_matches_device_forward():
             assert torch.equal(oh, r)
     finally:
         layer.close()
+
+
+
+def _random_workload(i):
+    """Seeded random shapes (multiples of 64 where the tensor-core path needs
+    them), covering both GEMM paths and ragged token counts."""
+    rng = np.random.default_rng(1000 + i)
+    E = int(rng.integers(2, 48))
+    k = int(rng.integers(1, min(E, 8) + 1))
+    t_max = 900 if i % 2 == 0 else 120     # odd cases small: the single-CTA GEMM path
+    return W(f"random{i}", T=int(rng.integers(1, t_max)), d=64 * int(rng.integers(1, 9)), E=E,
+             I=64 * int(rng.integers(1, 5)), Is=64 * int(rng.integers(0, 4)), k=k,
+             routed_scale=float(rng.choice([1.0, 2.5])), dtype="bf16")
+
+
+@pytest.mark.parametrize("i", range(4))
+def test_random_shapes_match_oracle(i):
+    w = _random_workload(i)
+    stats, rt = full_check(w)
+    print(w, stats, rt)
