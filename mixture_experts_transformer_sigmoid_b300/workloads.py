@@ -14,7 +14,8 @@ Recipe (every tensor has its own generator so that two workloads with the
 same weight shapes share the same weights, e.g. GLM-5 prefill and decode):
 
   tensor index:  x=0, norm_w=1, router_w=2, corr_bias=3, gate_up=4, down=5,
-                 shared_gate=6, shared_up=7, shared_down=8, hot_experts=9
+                 shared_gate=6, shared_up=7, shared_down=8, hot_experts=9,
+                 dense_gate=10, dense_up=11, dense_down=12
   generator seed: seed * 16 + tensor index
 
   x ~ N(0, 1); norm_w ~ U(0.5, 1.5); all projection weights ~ N(0, 0.02);
@@ -22,6 +23,12 @@ same weight shapes share the same weights, e.g. GLM-5 prefill and decode):
   plus +0.5 on ``n_hot`` experts taken from randperm(E)[:n_hot] when the
   workload is skewed.  gate_up / down are drawn one expert at a time.
   Values are drawn in fp32 and rounded (RNE) to the storage dtype.
+
+The dense feed-forward block of the first decoder layers (GlmMoeDsaMLP with
+its RMSNorm and residual) has workloads of its own (``DENSE_WORKLOADS``):
+the same x and norm_w recipe, and nn.Linear gate, up [I, d] and down [d, I]
+weights ~ N(0, 0.02).  The pages do not print GLM-5's dense intermediate
+size; the GLM-5-sized dense workloads take I = 2 d = 12288.
 """
 from __future__ import annotations
 
@@ -33,7 +40,7 @@ import torch
 TENSOR_INDEX = {
     "x": 0, "norm_w": 1, "router_w": 2, "corr_bias": 3, "gate_up": 4,
     "down": 5, "shared_gate": 6, "shared_up": 7, "shared_down": 8,
-    "hot_experts": 9,
+    "hot_experts": 9, "dense_gate": 10, "dense_up": 11, "dense_down": 12,
 }
 
 
@@ -94,6 +101,37 @@ WORKLOADS: Dict[str, Workload] = {
     "glm5_routing": Workload("glm5_routing", T=8192, d=6144, E=256, I=64,
                              Is=64, k=8, routed_scale=2.5, dtype="bf16",
                              description="T8192 d6144 E256 I64 k8 bf16"),
+}
+
+
+@dataclasses.dataclass(frozen=True)
+class DenseWorkload:
+    name: str
+    T: int                  # tokens
+    d: int                  # hidden size
+    I: int                  # intermediate size of the dense MLP
+    dtype: str              # "fp32" or "bf16"
+    eps: float = 1e-6
+    description: str = ""
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float32 if self.dtype == "fp32" else torch.bfloat16
+
+    def with_(self, **kw) -> "DenseWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+DENSE_WORKLOADS: Dict[str, DenseWorkload] = {
+    "dense_tiny_fp32": DenseWorkload("dense_tiny_fp32", T=40, d=256, I=384, dtype="fp32",
+                                     description="T40 d256 I384 fp32"),
+    "dense_small_bf16": DenseWorkload("dense_small_bf16", T=700, d=1024, I=1536, dtype="bf16",
+                                      description="T700 d1024 I1536 bf16"),
+    "glm5_dense_prefill": DenseWorkload("glm5_dense_prefill", T=8192, d=6144, I=12288,
+                                        dtype="bf16",
+                                        description="T8192 d6144 I12288 bf16"),
+    "glm5_dense_decode": DenseWorkload("glm5_dense_decode", T=64, d=6144, I=12288,
+                                       dtype="bf16", description="T64 d6144 I12288 bf16"),
 }
 
 
@@ -158,6 +196,29 @@ def make_inputs(w: Workload, seed: int = 0, device: str = "cpu",
         hot = torch.randperm(w.E, generator=gh, device=device)[: w.n_hot]
         bias[hot] += w.hot_bias
     out["corr_bias"] = bias.to(torch.float32).contiguous()
+    return out
+
+
+def make_dense_inputs(w: DenseWorkload, seed: int = 0, device: str = "cpu",
+                      T: Optional[int] = None,
+                      weights_from: Optional[Dict[str, torch.Tensor]] = None
+                      ) -> Dict[str, torch.Tensor]:
+    """Draw every input of one dense-block forward: x, norm_w, dense_gate,
+    dense_up [I, d] and dense_down [d, I] (the same conventions as
+    ``make_inputs``)."""
+    T = w.T if T is None else T
+    dt = w.torch_dtype
+    out: Dict[str, torch.Tensor] = {}
+    out["x"] = _normal((T, w.d), 1.0, _gen(seed, "x", device), device, dt)
+    if weights_from is not None:
+        for n in ("norm_w", "dense_gate", "dense_up", "dense_down"):
+            out[n] = weights_from[n]
+        return out
+    g = _gen(seed, "norm_w", device)
+    out["norm_w"] = (torch.rand(w.d, generator=g, device=device) + 0.5).to(dt)
+    out["dense_gate"] = _normal((w.I, w.d), 0.02, _gen(seed, "dense_gate", device), device, dt)
+    out["dense_up"] = _normal((w.I, w.d), 0.02, _gen(seed, "dense_up", device), device, dt)
+    out["dense_down"] = _normal((w.d, w.I), 0.02, _gen(seed, "dense_down", device), device, dt)
     return out
 
 

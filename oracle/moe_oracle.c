@@ -290,6 +290,44 @@ int oracle_forward(const oracle_cfg* c, int64_t n, const int64_t* rows,
     return failed ? 2 : 0;
 }
 
+/* The dense feed-forward block of the first first_k_dense_replace decoder
+ * layers (GLM-5 shared-expert page: GlmMoeDsaDecoderLayer.forward's second
+ * half with GlmMoeDsaMLP as the mlp):
+ *   out = x + down(silu(gate(xn)) * up(xn)),  xn = RMSNorm(x)  (step A),
+ * with nn.Linear weights gate, up [Is, d] and down [d, Is]; c->Is is the
+ * block's intermediate size, c->E, c->I and c->k are not used. */
+int oracle_dense_forward(const oracle_cfg* c, int64_t n, const int64_t* rows, const void* x,
+                         const void* gain, const void* gate, const void* up, const void* down,
+                         float* out, float* xn_out) {
+    if (!c || !x || !gain || !gate || !up || !down || !out || n < 0 || c->d < 1 || c->Is < 1)
+        return 1;
+    const int d = c->d;
+    int failed = 0;
+#pragma omp parallel
+    {
+        float* xn = (float*)malloc(sizeof(float) * d);
+        double* acc = (double*)malloc(sizeof(double) * d);
+        double* h = (double*)malloc(sizeof(double) * c->Is);
+        if (!xn || !acc || !h) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t t = 0; t < n; ++t) {
+                int64_t row = rows ? rows[t] : t;
+                rmsnorm_row(c, x, row, gain, xn);
+                for (int o = 0; o < d; ++o) acc[o] = 0.0;
+                shared_expert(c, xn, gate, up, down, acc, h);
+                for (int o = 0; o < d; ++o)
+                    out[t * d + o] = (float)((double)get(x, row * d + o, c->dtype) + acc[o]);
+                if (xn_out) memcpy(xn_out + t * d, xn, sizeof(float) * d);
+            }
+        }
+        free(xn); free(acc); free(h);
+    }
+    return failed ? 2 : 0;
+}
+
 int64_t oracle_param_count(const oracle_cfg* c) {
     int64_t d = c->d, E = c->E, I = c->I, Is = c->Is;
     int64_t routed = E * d * 2 * I + E * I * d;       /* gate_and_up_projs + down_projs */

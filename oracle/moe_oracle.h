@@ -23,6 +23,7 @@
  *      sh = Ds @ (silu(Gs @ xn) * (Us @ xn))
  *   I  out = x + sh + sum_j w_j * y_j   (GlmMoeDsaDecoderLayer.forward,
  *      second residual add)
+ * and, for the dense layers, out = x + GlmMoeDsaMLP(xn) (oracle_dense_forward).
  *
  * Precision: inputs are read exactly (bf16 bit patterns widened to fp32);
  * sums run in fp64 and are rounded to fp32 at the step boundaries above.
@@ -76,6 +77,14 @@ int oracle_forward(const oracle_cfg* c, int64_t n, const int64_t* rows,
                    const void* shared_gate, const void* shared_up, const void* shared_down,
                    const int32_t* forced_idx,
                    float* out, int32_t* idx, float* w, float* margin, float* xn, float* logits);
+
+/* The dense feed-forward block (GlmMoeDsaMLP with the residual), for the
+ * rows listed in `rows` (NULL = rows 0..n-1 of x): out [n, d] fp32 =
+ * x + down(silu(gate(xn)) * up(xn)), xn = step A.  gate, up [Is, d] and
+ * down [d, Is] (nn.Linear); Is = c->Is >= 1.  xn [n, d] may be NULL. */
+int oracle_dense_forward(const oracle_cfg* c, int64_t n, const int64_t* rows, const void* x,
+                         const void* gain, const void* gate, const void* up, const void* down,
+                         float* out, float* xn);
 
 /* Number of learned values and buffers the sublayer reads, RMSNorm gain excluded:
  * E*d*2I + E*I*d + 3*d*Is + E*d + E. */

@@ -56,10 +56,13 @@ def load():
         lib.oracle_forward.argtypes = [ctypes.POINTER(OracleCfg), ctypes.c_int64, P,
                                        P, P, P, P, P, P, P, P, P, P,
                                        P, P, P, P, P, P]
+        lib.oracle_dense_forward.argtypes = [ctypes.POINTER(OracleCfg), ctypes.c_int64, P,
+                                             P, P, P, P, P, P, P]
         lib.oracle_param_count.argtypes = [ctypes.POINTER(OracleCfg)]
         lib.oracle_param_count.restype = ctypes.c_int64
         lib.oracle_num_threads.restype = ctypes.c_int
-        for f in (lib.oracle_rmsnorm, lib.oracle_route, lib.oracle_select, lib.oracle_forward):
+        for f in (lib.oracle_rmsnorm, lib.oracle_route, lib.oracle_select, lib.oracle_forward,
+                  lib.oracle_dense_forward):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -148,6 +151,27 @@ def forward(c: OracleCfg, a: dict, rows: Optional[np.ndarray] = None,
         _ptr(a.get("shared_gate")), _ptr(a.get("shared_up")), _ptr(a.get("shared_down")),
         _ptr(forced), _ptr(res["out"]), _ptr(res["idx"]), _ptr(res["w"]),
         _ptr(res["margin"]), _ptr(res["xn"]), _ptr(res["logits"]))
+    assert rc == 0, rc
+    return res
+
+
+def dense_cfg(d: int, inter: int, dtype, eps: float = 1e-6) -> OracleCfg:
+    """Configuration of the dense block: ``inter`` travels in the Is field."""
+    return cfg(d, 1, 1, inter, 1, dtype, eps)
+
+
+def dense_forward(c: OracleCfg, a: dict, rows: Optional[np.ndarray] = None):
+    """The dense feed-forward block x + GlmMoeDsaMLP(RMSNorm(x)).  ``a``
+    holds host arrays as stored: x, norm_w, dense_gate, dense_up, dense_down.
+    Returns out and xn (fp32) for the selected rows."""
+    _check_storage(c, a["x"], a["norm_w"], a["dense_gate"], a["dense_up"], a["dense_down"])
+    n = a["x"].shape[0] if rows is None else len(rows)
+    rows_arr = None if rows is None else np.ascontiguousarray(rows, np.int64)
+    res = {"out": np.empty((n, c.d), np.float32), "xn": np.empty((n, c.d), np.float32)}
+    rc = load().oracle_dense_forward(
+        ctypes.byref(c), n, _ptr(rows_arr), _ptr(a["x"]), _ptr(a["norm_w"]),
+        _ptr(a["dense_gate"]), _ptr(a["dense_up"]), _ptr(a["dense_down"]),
+        _ptr(res["out"]), _ptr(res["xn"]))
     assert rc == 0, rc
     return res
 

@@ -402,3 +402,59 @@ def test_select_from_logits_matches_bruteforce(E, k):
     np.testing.assert_array_equal(idx2, idx3)
     np.testing.assert_array_equal(w2, w3)
     np.testing.assert_array_equal(m2, m3)
+
+
+# ---------------------------------------------------------------------------
+# The dense feed-forward block of the first decoder layers: the decoder-layer
+# excerpt on the GLM-5 shared-expert page applies post_attention_layernorm,
+# then GlmMoeDsaMLP, then the residual add.  Pinned against the MLP formula
+# written out in numpy (fp64) on the oracle's pinned RMSNorm output.
+# ---------------------------------------------------------------------------
+def dense_inputs(rng, T, d, I, dtype):
+    a = {
+        "x": rng.standard_normal((T, d)).astype(np.float32),
+        "norm_w": rng.uniform(0.5, 1.5, d).astype(np.float32),
+        "dense_gate": (rng.standard_normal((I, d)) * 0.1).astype(np.float32),
+        "dense_up": (rng.standard_normal((I, d)) * 0.1).astype(np.float32),
+        "dense_down": (rng.standard_normal((d, I)) * 0.1).astype(np.float32),
+    }
+    if dtype == "bf16":
+        a = {k: bf16_bits(v) for k, v in a.items()}
+    return a
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_dense_block_is_residual_plus_swiglu_mlp(dtype):
+    rng = np.random.default_rng(31)
+    T, d, I = 20, 64, 96          # I != d: a transposed weight reads the wrong values
+    a = dense_inputs(rng, T, d, I, dtype)
+    c = orc.dense_cfg(d, I, dtype)
+    r = orc.dense_forward(c, a)
+    np.testing.assert_array_equal(r["xn"], orc.rmsnorm(c, a["x"], a["norm_w"]))
+    xn = r["xn"].astype(np.float64)
+    G, U, Dl = (as_f64(a[n], dtype) for n in ("dense_gate", "dense_up", "dense_down"))
+    y = dense_swiglu(xn, G, U, Dl)
+    x64 = as_f64(a["x"], dtype)
+    np.testing.assert_allclose(r["out"], (x64 + y).astype(np.float32), rtol=1e-6, atol=1e-6)
+    # the gate is the projection inside silu: swapping gate and up changes the result
+    y_swapped = dense_swiglu(xn, U, G, Dl)
+    assert np.abs(y_swapped - y).max() > 100 * np.abs(r["out"] - (x64 + y)).max() + 1e-6
+
+
+def test_dense_block_zero_down_returns_the_residual():
+    rng = np.random.default_rng(32)
+    T, d, I = 8, 32, 48
+    a = dense_inputs(rng, T, d, I, "fp32")
+    a["dense_down"][:] = 0.0
+    r = orc.dense_forward(orc.dense_cfg(d, I, "fp32"), a)
+    np.testing.assert_array_equal(r["out"], a["x"])
+
+
+def test_dense_block_rows_are_independent():
+    rng = np.random.default_rng(33)
+    T, d, I = 12, 32, 40
+    a = dense_inputs(rng, T, d, I, "bf16")
+    c = orc.dense_cfg(d, I, "bf16")
+    full = orc.dense_forward(c, a)["out"]
+    rows = np.array([11, 0, 5, 5], np.int64)
+    np.testing.assert_array_equal(orc.dense_forward(c, a, rows=rows)["out"], full[rows])
