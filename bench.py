@@ -2,7 +2,8 @@
 """Throughput of the GLM MoE feed-forward sublayer forward pass on B300.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload glm5_prefill] [--no-decode] [--no-cpu-baseline]
+                  [--workload glm5_prefill] [--no-decode] [--no-dense] [--only-dense]
+                  [--no-cpu-baseline]
 
 One step is one forward pass of the whole sublayer (RMSNorm, sigmoid router
 and top-k, permutation, routed SwiGLU experts, shared expert, combine and
@@ -12,6 +13,10 @@ Per-stage times come from a second, directly launched pass of the same steps.  W
 N > 1 (launched by torch.distributed.run) every rank holds a full replica of
 the weights and runs its own batch: no collective is on the data path, so
 scaling is weak and the value is the tokens of all ranks per second.
+
+On the GLM-5 prefill workload the line also carries the GLM-5-shaped decode
+step (``decode``) and the dense feed-forward block of the first decoder
+layers (``dense``: moe_dense_forward at T = 8192 and T = 64).
 
 Rank 0 prints one JSON line.  ``--impl reference`` times the CPU oracle (the
 plain definition of the sublayer, run on the host cores) on a bounded sample
@@ -309,6 +314,10 @@ def run_ours(args, world, rank, local):
     if args.decode and w.name == "glm5_prefill":
         res["decode"] = run_decode(args, inp, local, peaks, peak_src, world)
 
+    # ---- the dense feed-forward block of the first decoder layers (moe_dense_forward)
+    if args.dense and w.name == "glm5_prefill":
+        res["dense"] = run_dense(args, local, peaks, peak_src, world)
+
     # ---- end to end: host buffers through the public host-I/O calls.  Every
     # step copies its batch in from pinned host memory and its result back.
     # moe_forward_host_async pipelines the copies against the neighbouring
@@ -418,6 +427,74 @@ def run_decode(args, inp3, local, peaks, peak_src, world):
             "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}}
 
 
+def run_dense(args, local, peaks, peak_src, world):
+    """moe_dense_forward on the GLM-5-sized dense block: prefill (T = 8192,
+    against the bf16 peak) and decode (T = 64, L2 flushed, against HBM)."""
+    from mixture_experts_transformer_sigmoid_b300 import binding as B
+    wp = wl.DENSE_WORKLOADS["glm5_dense_prefill"]
+    wd = wl.DENSE_WORKLOADS["glm5_dense_decode"]
+    inp = wl.make_dense_inputs(wp, device="cuda")
+    dinp = wl.make_dense_inputs(wd, device="cuda", weights_from=inp)
+    layer = B.MoeSublayer(max_tokens=wp.T, hidden=wp.d, n_experts=0, inter=0, shared_inter=0,
+                          max_top_k=0, dtype=wp.dtype, eps=wp.eps, device=local, dense_inter=wp.I)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for w, x in ((wp, inp["x"]), (wd, dinp["x"])):
+        out = torch.empty_like(x)
+        for _ in range(args.warmup):
+            layer.dense_forward(x, inp, out=out)
+        assert layer.sync_status() == B.MOE_OK
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            layer.dense_forward(x, inp, out=out)
+        torch.cuda.synchronize()
+        wbytes = 3 * w.d * w.I * 2
+        if w.T >= 1024:
+            # weights (453 MB) and activations exceed L2: no flush between steps
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.steps
+            flops = 6 * w.T * w.d * w.I
+            tf = flops / (ms / 1e3) / 1e12
+            res["prefill"] = {
+                "workload": w.name, "tokens": w.T, "ms_per_step": round(ms, 4),
+                "tokens_per_s": round(world * w.T / (ms / 1e3), 1), "flops_per_step": flops,
+                "tflops": round(tf, 1), "tensor_frac": round(tf / peaks["bf16_tflops"], 4),
+                "tensor_frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+                "peak_source": f"{peak_src} bf16 dense (burst)",
+                "launch": "CUDA graph replay of one moe_dense_forward (3 kernels)"}
+        else:
+            flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+            n_iter = max(50, args.steps * 4)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n_iter)]
+            for a, b in evs:
+                flush.zero_()
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms = statistics.median([a.elapsed_time(b) for a, b in evs])
+            nbytes = wbytes + 2 * w.T * w.d * 2 + w.d * 2
+            gbs = nbytes / (ms / 1e3) / 1e9
+            res["decode"] = {
+                "workload": w.name, "tokens": w.T, "ms_per_step_median": round(ms, 4),
+                "tokens_per_s": round(world * w.T / (ms / 1e3), 1), "bytes_per_step": nbytes,
+                "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                "peak_source": f"{peak_src} HBM copy",
+                "l2": "256 MB buffer written between steps (outside the timed events)",
+                "launch": "CUDA graph replay of one moe_dense_forward (3 kernels)"}
+        assert layer.sync_status() == B.MOE_OK
+        del graph
+    layer.close()
+    return res
+
+
 # ------------------------------------------------------------ reference arm
 def run_reference(args, world):
     """The CPU oracle on the host cores, on bounded samples of the workload."""
@@ -460,6 +537,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="glm5_prefill", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--no-decode", dest="decode", action="store_false")
+    ap.add_argument("--no-dense", dest="dense", action="store_false")
+    ap.add_argument("--only-dense", action="store_true",
+                    help="time only the dense feed-forward block (about 1 GB on the device; "
+                         "the case for profiling its kernels)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--ref-budget-s", type=float, default=150.0,
                     help="reference arm: seconds of oracle work for the whole run")
@@ -473,6 +554,22 @@ def main():
             print(json.dumps(run_reference(args, world)), flush=True)
         return
     world, rank, local = dist_setup()
+    if args.only_dense:
+        peaks, peak_src = load_peaks()
+        torch.cuda.set_device(local)
+        dense = run_dense(args, local, peaks, peak_src, world)
+        if rank == 0:
+            pf = dense["prefill"]
+            print(json.dumps({"metric": "dense feed-forward block tokens/s (glm5_dense_prefill)",
+                              "value": pf["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+                              "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": pf["ms_per_step"], "higher_is_better": True,
+                              "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
+                              "dense": dense}), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     res = run_ours(args, world, rank, local)
     if rank == 0:
         print(json.dumps(res), flush=True)

@@ -66,7 +66,8 @@ typedef enum { MOE_DTYPE_FP32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
 typedef struct {
     int32_t max_tokens;    /* largest T a forward may use (workspace sizing), >= 1 */
     int32_t hidden;        /* d */
-    int32_t n_experts;     /* E, 1..1024 */
+    int32_t n_experts;     /* E, 1..1024; 0 makes a handle for moe_dense_forward only
+                              (then inter, shared_inter and max_top_k must be 0) */
     int32_t inter;         /* I, routed expert intermediate size */
     int32_t shared_inter;  /* Is, shared expert intermediate size; 0 = no shared expert */
     int32_t max_top_k;     /* largest top_k a forward may use, 1..min(E, 32) */
@@ -75,11 +76,15 @@ typedef struct {
     int32_t device;        /* CUDA device ordinal */
     int32_t gemm_path;     /* 0 = automatic (tensor cores for bf16); 1 = force the
                               CUDA-core (FFMA) expert kernels (the fp32 path) */
+    int32_t dense_inter;   /* largest intermediate size moe_dense_forward may use;
+                              0 = the handle has no dense workspace */
 } moe_config;
 
 /* Creates a handle on cfg->device and allocates its workspace for
- * max_tokens * max_top_k routed rows.  bf16 handles on the tensor-core path
- * need hidden, inter and shared_inter to be multiples of 64
+ * max_tokens * max_top_k routed rows (and max_tokens * dense_inter values
+ * for moe_dense_forward).  bf16 handles on the tensor-core path need hidden,
+ * inter, shared_inter and dense_inter to be multiples of 64; the CUDA-core
+ * path needs hidden, inter, shared_inter and dense_inter <= 12288
  * (MOE_ERR_UNSUPPORTED otherwise).  *out is set only on MOE_OK. */
 MOE_API moe_status moe_init(const moe_config* cfg, moe_handle** out);
 
@@ -137,6 +142,25 @@ MOE_API moe_status moe_forward_host_async(moe_handle* h, int32_t T, const void* 
  * results are then in the callers' out_host buffers) and reports the device
  * error flag like moe_sync_status. */
 MOE_API moe_status moe_forward_host_wait(moe_handle* h);
+
+/* The dense feed-forward block of the first first_k_dense_replace decoder
+ * layers (GlmMoeDsaDecoderLayer.forward's second half with GlmMoeDsaMLP as
+ * the mlp, GLM-5 shared-expert page on OpenModelAtlas), per token:
+ *   out = x + down_w @ (silu(gate_w @ xn) * (up_w @ xn)),  xn = RMSNorm(x)
+ * with the same RMSNorm as moe_forward and nn.Linear weights:
+ *   x [T, d], norm_w [d], gate_w [inter, d], up_w [inter, d],
+ *   down_w [d, inter], out [T, d]   (device pointers, 16-byte aligned;
+ *   out must not overlap any input)
+ * 1 <= inter <= cfg.dense_inter, 0 <= T <= max_tokens (T == 0 queues
+ * nothing and reads no pointer).  The residual is added to the down
+ * projection's fp32 accumulator and rounded once.  Asynchronous on `stream`,
+ * no allocation, no host synchronisation; a device-side timeout is reported
+ * by moe_sync_status.  It reuses the handle's RMSNorm buffer (MOE_T_XN),
+ * which then holds the dense block's values; the per-stage times of moe_read_stats cover
+ * moe_forward only (the launch count includes both). */
+MOE_API moe_status moe_dense_forward(moe_handle* h, int32_t T, const void* x, const void* norm_w,
+                             const void* gate_w, const void* up_w, const void* down_w,
+                             int32_t inter, void* out, void* stream);
 
 /* Routing of the last forward on this handle, copied (device to device, on
  * `stream`) into caller buffers; any pointer may be NULL:

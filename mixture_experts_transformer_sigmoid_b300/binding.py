@@ -22,7 +22,7 @@ T_XN, T_LOGITS, T_OFFSETS, T_POS, T_ROW_TOK, T_H, T_SHARED = range(7)
 
 # Functions the header declares (kept in sync by the ABI test).
 EXPORTS = ("moe_init", "moe_forward", "moe_forward_host", "moe_forward_host_async",
-           "moe_forward_host_wait", "moe_get_routing",
+           "moe_forward_host_wait", "moe_dense_forward", "moe_get_routing",
            "moe_get_intermediate", "moe_sync_status", "moe_set_profiling", "moe_read_stats",
            "moe_destroy", "moe_route_static", "moe_status_string")
 STAGES = ("rmsnorm", "router", "topk", "scan", "scatter", "gather", "gate_up_swiglu",
@@ -34,7 +34,8 @@ class MoeConfig(ctypes.Structure):
                 ("n_experts", ctypes.c_int32), ("inter", ctypes.c_int32),
                 ("shared_inter", ctypes.c_int32), ("max_top_k", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("eps", ctypes.c_float),
-                ("device", ctypes.c_int32), ("gemm_path", ctypes.c_int32)]
+                ("device", ctypes.c_int32), ("gemm_path", ctypes.c_int32),
+                ("dense_inter", ctypes.c_int32)]
 
 
 class MoeStats(ctypes.Structure):
@@ -67,6 +68,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_forward_host.argtypes = fwd
     lib.moe_forward_host_async.argtypes = fwd
     lib.moe_forward_host_wait.argtypes = [P]
+    lib.moe_dense_forward.argtypes = [P, I32, P, P, P, P, P, I32, P, P]
     lib.moe_get_routing.argtypes = [P, P, P, P, P]
     lib.moe_get_intermediate.argtypes = [P, ctypes.c_int, P, ctypes.c_size_t, P]
     lib.moe_sync_status.argtypes = [P, P]
@@ -100,10 +102,11 @@ class MoeSublayer:
 
     def __init__(self, *, max_tokens: int, hidden: int, n_experts: int, inter: int,
                  shared_inter: int, max_top_k: int, dtype: str = "bf16", eps: float = 1e-6,
-                 device: int = 0, gemm_path: int = 0):
+                 device: int = 0, gemm_path: int = 0, dense_inter: int = 0):
         self.lib = load_library()
         self.cfg = MoeConfig(max_tokens, hidden, n_experts, inter, shared_inter, max_top_k,
-                             DTYPE_BF16 if dtype == "bf16" else DTYPE_FP32, eps, device, gemm_path)
+                             DTYPE_BF16 if dtype == "bf16" else DTYPE_FP32, eps, device, gemm_path,
+                             dense_inter)
         self.dtype = torch.bfloat16 if dtype == "bf16" else torch.float32
         self.device = torch.device("cuda", device)
         h = ctypes.c_void_p()
@@ -142,6 +145,18 @@ class MoeSublayer:
             _ptr(w.get("shared_up")), _ptr(w.get("shared_down")), top_k, routed_scale,
             _ptr(out), st), "moe_forward")
         self.last_T, self.last_k = T, top_k
+        return out
+
+    def dense_forward(self, x, w: dict, out=None, stream=None):
+        """moe_dense_forward: x + GlmMoeDsaMLP(RMSNorm(x)); w holds norm_w,
+        dense_gate, dense_up [I, d] and dense_down [d, I] (device tensors)."""
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty_like(x)
+        _check(self.lib.moe_dense_forward(
+            self.handle, T, _ptr(x), _ptr(w["norm_w"]), _ptr(w["dense_gate"]), _ptr(w["dense_up"]),
+            _ptr(w["dense_down"]), w["dense_gate"].shape[0], _ptr(out), self._stream(stream)),
+            "moe_dense_forward")
         return out
 
     def forward_host(self, x_host, w: dict, top_k: int, routed_scale: float, out_host,

@@ -347,9 +347,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_pair_kernel(const __gri
                         }
                     }
                     named_bar_sync(2, 128);
-                } else if constexpr (EPI == EPI_WEIGHTED) {
+                } else {
                     // stage this warp's 32 features x 32 tokens, then write 8 features of
-                    // one token per 16-byte store, scaled by that token's routing weight
+                    // one token per 16-byte store: scaled by that token's routing weight
+                    // (EPI_WEIGHTED) or added to 8 residual values read with one
+                    // 16-byte load (EPI_RESIDUAL)
+                    static_assert(EPI == EPI_WEIGHTED || EPI == EPI_RESIDUAL, "epilogue");
                     float* stg = xbuf + q * (32 * 33);
 #pragma unroll
                     for (int c = 0; c < 32; ++c) stg[c * 33 + lane] = __uint_as_float(v[c]);
@@ -361,13 +364,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_pair_kernel(const __gri
                         const int t = r * 8 + (lane >> 2);       // bank = t + 8 * sub: conflict-free
                         if (t < cmax && col < sg.F) {
                             const int row = ti.row0 + c0 + t;
-                            const float wv = sg.row_w ? sg.row_w[row] : 1.0f;
                             uint32_t pk[4];
+                            if constexpr (EPI == EPI_WEIGHTED) {
+                                const float wv = sg.row_w ? sg.row_w[row] : 1.0f;
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const __nv_bfloat162 hb = __floats2bfloat162_rn(
-                                    stg[t * 33 + sub * 8 + 2 * j] * wv, stg[t * 33 + sub * 8 + 2 * j + 1] * wv);
-                                pk[j] = *reinterpret_cast<const uint32_t*>(&hb);
+                                for (int j = 0; j < 4; ++j) {
+                                    const __nv_bfloat162 hb = __floats2bfloat162_rn(
+                                        stg[t * 33 + sub * 8 + 2 * j] * wv, stg[t * 33 + sub * 8 + 2 * j + 1] * wv);
+                                    pk[j] = *reinterpret_cast<const uint32_t*>(&hb);
+                                }
+                            } else {
+                                const uint4 r4 = *reinterpret_cast<const uint4*>(
+                                    static_cast<const __nv_bfloat16*>(sg.res) + static_cast<size_t>(row) * sg.ld_out + col);
+                                const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const float2 rf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rw[j]));
+                                    const __nv_bfloat162 hb = __floats2bfloat162_rn(rf.x + stg[t * 33 + sub * 8 + 2 * j],
+                                                                                    rf.y + stg[t * 33 + sub * 8 + 2 * j + 1]);
+                                    pk[j] = *reinterpret_cast<const uint32_t*>(&hb);
+                                }
                             }
                             *reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * sg.ld_out + col) =
                                 make_uint4(pk[0], pk[1], pk[2], pk[3]);

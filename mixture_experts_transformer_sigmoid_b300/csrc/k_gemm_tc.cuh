@@ -46,7 +46,10 @@ constexpr uint64_t TC_TIMEOUT_NS = 2000000000ull;   // 2 s
 constexpr uint64_t TC_DRAIN_NS = 100000000ull;      // 100 ms
 constexpr int DEVERR_TIMEOUT = 1;
 
-enum EpiKind { EPI_SWIGLU = 1, EPI_WEIGHTED = 2 };
+// SWIGLU: out = silu(gate) * up, from the gate and up halves of the A rows.
+// WEIGHTED: out = row_w[row] * acc (row_w null: acc).
+// RESIDUAL: out = res[row, col] + acc, added in fp32 and rounded once.
+enum EpiKind { EPI_SWIGLU = 1, EPI_WEIGHTED = 2, EPI_RESIDUAL = 3 };
 
 struct TcSeg {
     int grouped;          // 1: expert groups from offsets[]; 0: one group of n_rows rows
@@ -61,6 +64,8 @@ struct TcSeg {
     const float* row_w;   // weighted epilogue: per-row factor; null means 1
     int a_rank_off;       // CTA-pair kernel: feature offset of the second CTA's rows
     int a_kind;           // CTA-pair kernel: how a0 delivers the 128 A rows (PairAKind)
+    const void* res;      // residual epilogue: bf16 [rows, ld_out], indexed like out
+    int f_group;          // dense segment: feature tiles per tile group (0: all of them)
 };
 
 struct TcParams {
@@ -85,6 +90,11 @@ struct TileInfo {
 // A group of m rows is split evenly into ceil(m / BN) token tiles (e.g. 300
 // rows as 150 + 150, not 256 + 44): the same weight traffic, but no MMA with
 // a small N, whose fixed cost per instruction would dominate.
+// A dense segment whose weights do not fit in L2 orders its tiles in groups
+// of f_group feature tiles, token tile-major inside a group: the CTAs that
+// run together then share a few weight tiles and a few token tiles, and each
+// group's weights are read from DRAM once (token tile-major over all feature
+// tiles would stream every weight once per token tile).
 __device__ __forceinline__ bool decode_tile(const TcParams& p, const int* prefix, int L, int BN,
                                             TileInfo& ti) {
     for (int s = 0; s < p.n_segs; ++s) {
@@ -92,9 +102,18 @@ __device__ __forceinline__ bool decode_tile(const TcParams& p, const int* prefix
         const int ntok = sg.grouped ? prefix[p.E] : (sg.n_rows + BN - 1) / BN;
         const int cnt = ntok * sg.n_ftiles;
         if (L < cnt) {
-            const int tt = L / sg.n_ftiles;
+            int tt = L / sg.n_ftiles;
             ti.ftile = L - tt * sg.n_ftiles;
             ti.seg = s;
+            if (!sg.grouped && sg.f_group > 0 && sg.f_group < sg.n_ftiles) {
+                const int per_group = sg.f_group * ntok;
+                const int g = L / per_group;
+                const int f_first = g * sg.f_group;
+                const int gf = min(sg.f_group, sg.n_ftiles - f_first);
+                const int within = L - g * per_group;
+                tt = within / gf;
+                ti.ftile = f_first + (within - tt * gf);
+            }
             if (sg.grouped) {
                 int lo = 0, hi = p.E;  // prefix[lo] <= tt < prefix[hi]
                 while (hi - lo > 1) {
@@ -368,6 +387,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                             const float wv = sg.row_w ? sg.row_w[row] : 1.0f;
                             out[static_cast<size_t>(row) * sg.ld_out + col] =
                                 __float2bfloat16_rn(__uint_as_float(v[c]) * wv);
+                        }
+                    }
+                } else if constexpr (EPI == EPI_RESIDUAL) {
+                    const int col = ti.ftile * sg.a_fstride + q * 32 + lane;
+                    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
+                    const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(sg.res);
+                    if (col < sg.F) {
+                        const int cmax = min(32, ti.rows - c0);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            if (c >= cmax) break;
+                            const size_t at = static_cast<size_t>(ti.row0 + c0 + c) * sg.ld_out + col;
+                            out[at] = __float2bfloat16_rn(__bfloat162float(res[at]) + __uint_as_float(v[c]));
                         }
                     }
                 }

@@ -675,10 +675,12 @@ __global__ void simt_shared_gate_up_kernel(const T* __restrict__ xn, const T* __
     hs[static_cast<size_t>(t) * Is + i] = Elem<T>::from_f(silu_f(g) * u);
 }
 
-// sh[t, o] = Ds[o] . hs[t].
+// sh[t, o] = Ds[o] . hs[t], plus res[t, o] when res is not null (the dense
+// block's residual, added in fp32 before the one rounding).
 template <typename T>
 __global__ void simt_shared_down_kernel(const T* __restrict__ hs, const T* __restrict__ Ds,
-                                        int Is, int d, T* __restrict__ sh) {
+                                        int Is, int d, T* __restrict__ sh,
+                                        const T* __restrict__ res = nullptr) {
     extern __shared__ float rowv[];
     const int t = blockIdx.x;
     for (int i = threadIdx.x; i < Is; i += blockDim.x)
@@ -688,7 +690,9 @@ __global__ void simt_shared_down_kernel(const T* __restrict__ hs, const T* __res
     if (o >= d) return;
     float acc = 0.f;
     for (int i = 0; i < Is; ++i) acc = fmaf(Elem<T>::to_f(Ds[static_cast<size_t>(o) * Is + i]), rowv[i], acc);
-    sh[static_cast<size_t>(t) * d + o] = Elem<T>::from_f(acc);
+    const size_t at = static_cast<size_t>(t) * d + o;
+    if (res != nullptr) acc += Elem<T>::to_f(res[at]);
+    sh[at] = Elem<T>::from_f(acc);
 }
 
 }  // namespace moe

@@ -9,6 +9,10 @@
 //   combine with the residual.
 // fp32 storage (and gemm_path = 1) runs the same routing kernels with the
 // router fused into RMSNorm and the expert contractions on CUDA cores.
+//
+// Dense feed-forward block (moe_dense_forward): rmsnorm -> gate|up GEMM with
+// SwiGLU epilogue -> down GEMM with the residual added in its epilogue, on
+// the same two GEMM kernels (one dense segment each).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -55,6 +59,7 @@ struct moe_handle {
     void* yp = nullptr;
     void* hs = nullptr;
     void* sh = nullptr;
+    void* hd = nullptr;       // dense block activations [max_tokens, dense_inter]
     void* x_stage = nullptr;
     void* out_stage = nullptr;
     // pipelined host I/O (moe_forward_host_async): a second staging slot, copy
@@ -151,7 +156,8 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 void free_ws(moe_handle* h) {
     void* ptrs[] = {h->xn, h->logits, h->part, h->topk_idx, h->topk_w, h->chunk_cnt, h->chunk_base,
                     h->counts, h->offsets, h->pos, h->row_tok, h->row_w, h->xp, h->h, h->yp,
-                    h->hs, h->sh, h->x_stage, h->out_stage, h->x_stage2, h->out_stage2, h->err};
+                    h->hs, h->sh, h->hd, h->x_stage, h->out_stage, h->x_stage2, h->out_stage2,
+                    h->err};
     for (void* p : ptrs)
         if (p) cudaFree(p);
 }
@@ -204,6 +210,21 @@ int tile_bound(const TcParams& prm, int BN, int P) {
         n += ntok * sg.n_ftiles;
     }
     return static_cast<int>(std::min<int64_t>(n, 1 << 30));
+}
+
+// Tile groups of a dense segment (TcSeg::f_group): weights that fit in L2
+// with room to spare keep one group (plain token tile-major order); larger
+// ones are cut into groups of about 48 MB of weight rows.
+#ifndef MOE_DENSE_GROUP_MB
+#define MOE_DENSE_GROUP_MB 48
+#endif
+void set_dense_groups(TcSeg& sg, int weight_rows_per_ftile) {
+    const double ftile_bytes = 2.0 * weight_rows_per_ftile * sg.K;
+    if (ftile_bytes * sg.n_ftiles <= 64.0 * (1 << 20)) {
+        sg.f_group = 0;
+        return;
+    }
+    sg.f_group = std::max(1, static_cast<int>(MOE_DENSE_GROUP_MB * double(1 << 20) / ftile_bytes));
 }
 
 // CTA-pair grouped GEMM: as many clusters of two as the device keeps
@@ -413,6 +434,7 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
                 return MOE_ERR_CUDA;
             g1.seg[1] = pair ? TcSeg{0, Tn, d, 128, 0, (Is + 127) / 128, Is, Is, hs, nullptr, 64, PA_TWO_2D}
                              : TcSeg{0, Tn, d, 64, 0, Is / 64, Is, Is, hs, nullptr, 0, 0};
+            set_dense_groups(g1.seg[1], pair ? 256 : 128);
         }
         if (run_tc<EPI_SWIGLU>(g1, pair, P, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
         mark(h, 7, st);
@@ -443,11 +465,13 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
                     !map_2d(&g2.b128[1], hs, Is, Tn, 128))
                     return MOE_ERR_CUDA;
                 g2.seg[1] = TcSeg{0, Tn, Is, 256, 64, (d + 255) / 256, d, d, sh, nullptr, 128, PA_ONE_2D};
+                set_dense_groups(g2.seg[1], 256);
             } else {
                 if (!map_2d(&g2.a0[1], a.sd, Is, d) || !map_2d(&g2.a1[1], a.sd, Is, d) ||
                     !map_2d(&g2.b[1], hs, Is, Tn))
                     return MOE_ERR_CUDA;
                 g2.seg[1] = TcSeg{0, Tn, Is, 128, 64, (d + 127) / 128, d, d, sh, nullptr, 0, 0};
+                set_dense_groups(g2.seg[1], 128);
             }
         }
         if (run_tc<EPI_WEIGHTED>(g2, pair, P, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
@@ -473,6 +497,68 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     combine_kernel<T><<<Tn, 256, 0, st>>>(x, sh, yp, h->pos, d, k, static_cast<T*>(a.out));
     h->launches += 1;
     mark(h, moe_handle::NSTAGE, st);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Dense feed-forward block: RMSNorm, then gate|up with the SwiGLU epilogue
+// into hd, then down with the residual added to the fp32 result before its
+// one rounding (in the GEMM epilogue, or in the CUDA-core down kernel).
+template <typename T>
+moe_status dense_impl(moe_handle* h, int Tn, const void* x_, const void* norm_w, const void* gw,
+                      const void* uw, const void* dw, int Id, void* out, cudaStream_t st) {
+    const moe_config& c = h->cfg;
+    const int d = c.hidden;
+    const T* x = static_cast<const T*>(x_);
+    T* xn = static_cast<T*>(h->xn);
+    T* hd = static_cast<T*>(h->hd);
+    if (d / Elem<T>::V <= 32 * RMS_WARP_VECS && Tn >= 8 * h->num_sms)
+        rmsnorm_warp_kernel<T><<<(Tn + 7) / 8, 256, 0, st>>>(x, static_cast<const T*>(norm_w), xn, Tn, d,
+                                                             c.eps);
+    else
+        rmsnorm_kernel<T><<<Tn, 256, 0, st>>>(x, static_cast<const T*>(norm_w), xn, d, c.eps);
+    if (h->tc) {
+        // CTA pairs (256 x 256 tiles) from two 64-token tiles up
+        const bool pair = Tn >= 128;
+        TcParams g1;
+        std::memset(&g1, 0, sizeof g1);
+        g1.E = 1;
+        g1.offsets = h->offsets;
+        g1.err = h->err;
+        g1.n_segs = 1;
+        if (!map_2d(&g1.a0[0], gw, d, Id) || !map_2d(&g1.a1[0], uw, d, Id) || !map_2d(&g1.b[0], xn, d, Tn) ||
+            !map_2d(&g1.b128[0], xn, d, Tn, 128))
+            return MOE_ERR_CUDA;
+        g1.seg[0] = pair ? TcSeg{0, Tn, d, 128, 0, (Id + 127) / 128, Id, Id, hd, nullptr, 64, PA_TWO_2D, nullptr}
+                         : TcSeg{0, Tn, d, 64, 0, Id / 64, Id, Id, hd, nullptr, 0, 0, nullptr};
+        set_dense_groups(g1.seg[0], pair ? 256 : 128);
+        if (run_tc<EPI_SWIGLU>(g1, pair, Tn, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        TcParams g2;
+        std::memset(&g2, 0, sizeof g2);
+        g2.E = 1;
+        g2.offsets = h->offsets;
+        g2.err = h->err;
+        g2.n_segs = 1;
+        if (pair) {
+            if (!map_2d(&g2.a0[0], dw, Id, d, 128) || !map_2d(&g2.b[0], hd, Id, Tn) ||
+                !map_2d(&g2.b128[0], hd, Id, Tn, 128))
+                return MOE_ERR_CUDA;
+            g2.seg[0] = TcSeg{0, Tn, Id, 256, 64, (d + 255) / 256, d, d, out, nullptr, 128, PA_ONE_2D, x};
+            set_dense_groups(g2.seg[0], 256);
+        } else {
+            if (!map_2d(&g2.a0[0], dw, Id, d) || !map_2d(&g2.a1[0], dw, Id, d) || !map_2d(&g2.b[0], hd, Id, Tn))
+                return MOE_ERR_CUDA;
+            g2.seg[0] = TcSeg{0, Tn, Id, 128, 64, (d + 127) / 128, d, d, out, nullptr, 0, 0, x};
+            set_dense_groups(g2.seg[0], 128);
+        }
+        if (run_tc<EPI_RESIDUAL>(g2, pair, Tn, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        h->launches += 3;
+    } else {
+        simt_shared_gate_up_kernel<T><<<dim3(Tn, (Id + 127) / 128), 128, d * sizeof(float), st>>>(
+            xn, static_cast<const T*>(gw), static_cast<const T*>(uw), d, Id, hd);
+        simt_shared_down_kernel<T><<<dim3(Tn, (d + 127) / 128), 128, Id * sizeof(float), st>>>(
+            hd, static_cast<const T*>(dw), Id, d, static_cast<T*>(out), x);
+        h->launches += 3;
+    }
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -621,18 +707,26 @@ const char* moe_status_string(moe_status s) {
 moe_status moe_init(const moe_config* cfg, moe_handle** out) {
     if (!cfg || !out) return MOE_ERR_INVALID_ARG;
     const moe_config c = *cfg;
-    if (c.max_tokens < 1 || c.hidden < 1 || c.n_experts < 1 || c.n_experts > 1024 ||
-        c.inter < 1 || c.shared_inter < 0 || c.max_top_k < 1 || c.max_top_k > 32 ||
-        c.max_top_k > c.n_experts || (c.dtype != MOE_DTYPE_FP32 && c.dtype != MOE_DTYPE_BF16) ||
-        !(c.eps >= 0.0f) || !std::isfinite(c.eps) || c.device < 0 ||
-        (c.gemm_path != 0 && c.gemm_path != 1))
+    const bool dense_only = c.n_experts == 0;
+    const bool sizes_ok =
+        dense_only ? (c.inter == 0 && c.shared_inter == 0 && c.max_top_k == 0 && c.dense_inter >= 1)
+                   : (c.n_experts <= 1024 && c.inter >= 1 && c.shared_inter >= 0 && c.max_top_k >= 1 &&
+                      c.max_top_k <= 32 && c.max_top_k <= c.n_experts && c.dense_inter >= 0);
+    if (c.max_tokens < 1 || c.hidden < 1 || c.n_experts < 0 || !sizes_ok ||
+        (c.dtype != MOE_DTYPE_FP32 && c.dtype != MOE_DTYPE_BF16) || !(c.eps >= 0.0f) ||
+        !std::isfinite(c.eps) || c.device < 0 || (c.gemm_path != 0 && c.gemm_path != 1))
         return MOE_ERR_INVALID_ARG;
     const int es = c.dtype == MOE_DTYPE_BF16 ? 2 : 4;
     const int vec = 16 / es;  // 16-byte vectors in RMSNorm, gather and combine
-    if (c.hidden % vec != 0 || c.inter % vec != 0 || c.shared_inter % vec != 0)
+    if (c.hidden % vec != 0 || c.inter % vec != 0 || c.shared_inter % vec != 0 || c.dense_inter % vec != 0)
         return MOE_ERR_UNSUPPORTED;
     const bool tc = c.dtype == MOE_DTYPE_BF16 && c.gemm_path == 0;
-    if (tc && (c.hidden % 64 != 0 || c.inter % 64 != 0 || c.shared_inter % 64 != 0))
+    if (tc && (c.hidden % 64 != 0 || c.inter % 64 != 0 || c.shared_inter % 64 != 0 || c.dense_inter % 64 != 0))
+        return MOE_ERR_UNSUPPORTED;
+    // the CUDA-core contractions stage one input row of fp32 in 48 KB of shared memory
+    constexpr int FFMA_MAX_K = 48 * 1024 / 4;
+    if (!tc && (c.hidden > FFMA_MAX_K || c.inter > FFMA_MAX_K || c.shared_inter > FFMA_MAX_K ||
+                c.dense_inter > FFMA_MAX_K))
         return MOE_ERR_UNSUPPORTED;
     const int64_t P_max = static_cast<int64_t>(c.max_tokens) * c.max_top_k;
     if (P_max > (int64_t(1) << 31) - 1) return MOE_ERR_UNSUPPORTED;
@@ -680,10 +774,13 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out) {
     alloc(&h->yp, P * d * es);
     alloc(&h->hs, T * std::max<size_t>(Is, 1) * es);
     alloc(&h->sh, T * d * es);
-    alloc(&h->x_stage, T * d * es);
-    alloc(&h->out_stage, T * d * es);
-    alloc(&h->x_stage2, T * d * es);
-    alloc(&h->out_stage2, T * d * es);
+    if (c.dense_inter > 0) alloc(&h->hd, T * static_cast<size_t>(c.dense_inter) * es);
+    if (!dense_only) {   // host-I/O staging of moe_forward_host(_async)
+        alloc(&h->x_stage, T * d * es);
+        alloc(&h->out_stage, T * d * es);
+        alloc(&h->x_stage2, T * d * es);
+        alloc(&h->out_stage2, T * d * es);
+    }
     alloc(&h->err, 4);
     if (ok && cudaMemset(h->err, 0, 4) != cudaSuccess) ok = false;
     if (!ok) {
@@ -717,6 +814,30 @@ moe_status moe_forward(moe_handle* h, int32_t T, const void* x, const void* norm
     moe_status s = validate_forward(h, a, false);
     if (s != MOE_OK) return s;
     return forward_impl(h, a, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_dense_forward(moe_handle* h, int32_t T, const void* x, const void* norm_w,
+                             const void* gate_w, const void* up_w, const void* down_w,
+                             int32_t inter, void* out, void* stream) {
+    if (!h) return MOE_ERR_INVALID_ARG;
+    const moe_config& c = h->cfg;
+    if (T < 0 || T > c.max_tokens || inter < 1 || inter > c.dense_inter) return MOE_ERR_INVALID_ARG;
+    if (inter % (h->tc ? 64 : 16 / h->es) != 0) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;  // nothing is read or written
+    const void* ptrs[] = {x, norm_w, gate_w, up_w, down_w, out};
+    for (const void* p : ptrs)
+        if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    const size_t es = h->es, d = c.hidden, Id = inter;
+    const size_t out_b = static_cast<size_t>(T) * d * es;
+    const struct { const void* p; size_t n; } ins[] = {
+        {x, out_b}, {norm_w, d * es}, {gate_w, Id * d * es}, {up_w, Id * d * es}, {down_w, d * Id * es}};
+    for (const auto& in : ins)
+        if (overlaps(out, out_b, in.p, in.n)) return MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(c.device) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return c.dtype == MOE_DTYPE_BF16
+               ? dense_impl<__nv_bfloat16>(h, T, x, norm_w, gate_w, up_w, down_w, inter, out, st)
+               : dense_impl<float>(h, T, x, norm_w, gate_w, up_w, down_w, inter, out, st);
 }
 
 moe_status moe_forward_host(moe_handle* h, int32_t T, const void* x_host, const void* norm_w,

@@ -51,7 +51,7 @@ def test_status_strings(lib):
 
 def good_cfg(**kw):
     c = dict(max_tokens=64, hidden=256, n_experts=8, inter=128, shared_inter=128, max_top_k=2,
-             dtype=B.DTYPE_BF16, eps=1e-6, device=0, gemm_path=0)
+             dtype=B.DTYPE_BF16, eps=1e-6, device=0, gemm_path=0, dense_inter=0)
     c.update(kw)
     return B.MoeConfig(**c)
 
@@ -72,6 +72,18 @@ def good_cfg(**kw):
     (dict(hidden=200), B.MOE_ERR_UNSUPPORTED),       # tensor-core path needs multiples of 64
     (dict(inter=100), B.MOE_ERR_UNSUPPORTED),
     (dict(hidden=36, dtype=B.DTYPE_FP32), B.MOE_OK),                # valid fp32 shape
+    (dict(dense_inter=-1), B.MOE_ERR_INVALID_ARG),
+    (dict(dense_inter=100), B.MOE_ERR_UNSUPPORTED),  # tensor-core path needs multiples of 64
+    (dict(dense_inter=512), B.MOE_OK),               # MoE handle with dense workspace
+    # a handle for the dense block only: no experts, no routed sizes
+    (dict(n_experts=0, inter=0, shared_inter=0, max_top_k=0, dense_inter=512), B.MOE_OK),
+    (dict(n_experts=0, inter=0, shared_inter=0, max_top_k=0, dense_inter=0), B.MOE_ERR_INVALID_ARG),
+    (dict(n_experts=0, inter=128, shared_inter=0, max_top_k=0, dense_inter=512), B.MOE_ERR_INVALID_ARG),
+    (dict(n_experts=0, inter=0, shared_inter=0, max_top_k=1, dense_inter=512), B.MOE_ERR_INVALID_ARG),
+    # the CUDA-core path stages one fp32 input row in 48 KB of shared memory
+    (dict(dtype=B.DTYPE_FP32, dense_inter=12288), B.MOE_OK),
+    (dict(dtype=B.DTYPE_FP32, dense_inter=12292), B.MOE_ERR_UNSUPPORTED),
+    (dict(dtype=B.DTYPE_FP32, hidden=12800), B.MOE_ERR_UNSUPPORTED),
 ])
 def test_init_rejects_bad_config(lib, kw, status):
     c = good_cfg(**kw)
@@ -102,6 +114,7 @@ def test_calls_on_null_handle(lib):
     assert lib.moe_get_routing(None, None, None, None, None) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_get_intermediate(None, 0, p, 16, None) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_sync_status(None, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_dense_forward(None, 1, p, p, p, p, p, 64, p, None) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_destroy(None) == B.MOE_OK
 
 
