@@ -176,6 +176,21 @@ def dense_forward(c: OracleCfg, a: dict, rows: Optional[np.ndarray] = None):
     return res
 
 
+def pack_experts(gate: np.ndarray, up: np.ndarray, down: np.ndarray):
+    """HF per-expert nn.Linear weights -> the grouped native layout (NeMo
+    AutoModel GLM4-MoE state dict adapter page, Glm4MoeStateDictAdapter:
+    experts.{E}.gate_proj / up_proj / down_proj are grouped into
+    gate_and_up_projs [n_experts, dim, 2*moe_inter_dim] and down_projs
+    [n_experts, moe_inter_dim, dim]).  gate, up [E, I, d] and down [E, d, I]
+    are the experts' HF tensors stacked; gate_and_up[e] = [gate[e]^T | up[e]^T]
+    (gate columns first), down_projs[e] = down[e]^T.  Pure data movement: any
+    dtype, bit for bit."""
+    gate_up = np.ascontiguousarray(np.concatenate([gate.transpose(0, 2, 1), up.transpose(0, 2, 1)],
+                                                  axis=2))
+    down_projs = np.ascontiguousarray(down.transpose(0, 2, 1))
+    return gate_up, down_projs
+
+
 def param_count(c: OracleCfg) -> int:
     return int(load().oracle_param_count(ctypes.byref(c)))
 

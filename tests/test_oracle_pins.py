@@ -458,3 +458,41 @@ def test_dense_block_rows_are_independent():
     full = orc.dense_forward(c, a)["out"]
     rows = np.array([11, 0, 5, 5], np.int64)
     np.testing.assert_array_equal(orc.dense_forward(c, a, rows=rows)["out"], full[rows])
+
+
+# ---------------------------------------------------------------------------
+# HF -> grouped layout packing (state dict adapter page): the packed tensors,
+# fed to the sublayer oracle, give the SwiGLU MLP of the HF nn.Linear weights
+# (GlmMoeDsaMLP orientation, y = x W^T) for every expert.
+# ---------------------------------------------------------------------------
+def test_packed_layout_gives_the_hf_experts():
+    rng = np.random.default_rng(41)
+    T, d, E, I = 9, 32, 3, 24
+    G = (rng.standard_normal((E, I, d)) * 0.2).astype(np.float32)
+    U = (rng.standard_normal((E, I, d)) * 0.2).astype(np.float32)
+    Dn = (rng.standard_normal((E, d, I)) * 0.2).astype(np.float32)
+    gate_up, down = orc.pack_experts(G, U, Dn)
+    assert gate_up.shape == (E, d, 2 * I) and down.shape == (E, I, d)
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    for e in range(E):
+        # one expert at a time: top-1 over a single expert routes every token to it
+        a = {"x": x, "norm_w": np.ones(d, np.float32), "router_w": np.zeros((1, d), np.float32),
+             "corr_bias": np.zeros(1, np.float32), "gate_up": np.ascontiguousarray(gate_up[e:e + 1]),
+             "down": np.ascontiguousarray(down[e:e + 1])}
+        r = orc.forward(orc.cfg(d, 1, I, 0, 1, "fp32", routed_scale=1.0), a)
+        xn = r["xn"].astype(np.float64)
+        y = dense_swiglu(xn, G[e].astype(np.float64), U[e].astype(np.float64), Dn[e].astype(np.float64))
+        np.testing.assert_allclose(r["out"], (x + y).astype(np.float32), rtol=1e-6, atol=1e-6)
+
+
+def test_packing_is_exact_data_movement():
+    rng = np.random.default_rng(42)
+    E, d, I = 2, 5, 3
+    bits = rng.integers(0, 2 ** 16, size=(3, E, I, d), dtype=np.uint16)
+    G, U, Dn = bits[0], bits[1], bits[2].transpose(0, 2, 1).copy()
+    gate_up, down = orc.pack_experts(G, U, Dn)
+    for e in range(E):
+        for j in range(d):
+            for i in range(I):
+                assert gate_up[e, j, i] == G[e, i, j] and gate_up[e, j, I + i] == U[e, i, j]
+                assert down[e, i, j] == Dn[e, j, i]
