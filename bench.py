@@ -2,7 +2,7 @@
 """Throughput of the GLM MoE feed-forward sublayer forward pass on B300.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload glm5_prefill] [--no-decode] [--no-dense] [--only-dense]
+                  [--workload glm5_prefill] [--no-decode] [--no-dense] [--no-pack] [--only-dense]
                   [--no-cpu-baseline]
 
 One step is one forward pass of the whole sublayer (RMSNorm, sigmoid router
@@ -15,8 +15,9 @@ the weights and runs its own batch: no collective is on the data path, so
 scaling is weak and the value is the tokens of all ranks per second.
 
 On the GLM-5 prefill workload the line also carries the GLM-5-shaped decode
-step (``decode``) and the dense feed-forward block of the first decoder
-layers (``dense``: moe_dense_forward at T = 8192 and T = 64).
+step (``decode``), the dense feed-forward block of the first decoder
+layers (``dense``: moe_dense_forward at T = 8192 and T = 64) and the
+packing of the experts' HF weights into the grouped layout (``pack``).
 
 Rank 0 prints one JSON line.  ``--impl reference`` times the CPU oracle (the
 plain definition of the sublayer, run on the host cores) on a bounded sample
@@ -42,6 +43,7 @@ from mixture_experts_transformer_sigmoid_b300 import workloads as wl  # noqa: E4
 
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 METRIC = "MoE sublayer tokens/s"
+SWEEP_T = (1, 8, 16, 32, 128)   # decode token range (GLM-5 decode weights and bias)
 
 # DRAM bytes (read + write) per launch of the grouped GEMMs from the ncu
 # capture summarised in profiles/tc_gemm_pair_glm5_slice.md: the GLM-5 slice
@@ -318,6 +320,10 @@ def run_ours(args, world, rank, local):
     if args.dense and w.name == "glm5_prefill":
         res["dense"] = run_dense(args, local, peaks, peak_src, world)
 
+    # ---- HF -> grouped layout packing of the GLM-5 expert weights (moe_pack_experts)
+    if args.pack and w.name == "glm5_prefill":
+        res["pack"] = run_pack(args, inp, peaks, peak_src)
+
     # ---- end to end: host buffers through the public host-I/O calls.  Every
     # step copies its batch in from pinned host memory and its result back.
     # moe_forward_host_async pipelines the copies against the neighbouring
@@ -365,7 +371,7 @@ def run_decode(args, inp3, local, peaks, peak_src, world):
     from mixture_experts_transformer_sigmoid_b300 import binding as B
     w = wl.WORKLOADS["glm5_decode"]
     dinp = wl.make_inputs(w, seed=0, device="cuda", weights_from=inp3)
-    layer = B.MoeSublayer(max_tokens=w.T, hidden=w.d, n_experts=w.E, inter=w.I,
+    layer = B.MoeSublayer(max_tokens=max(SWEEP_T), hidden=w.d, n_experts=w.E, inter=w.I,
                           shared_inter=w.Is, max_top_k=w.k, dtype=w.dtype, eps=w.eps, device=local)
     out = torch.empty_like(dinp["x"])
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
@@ -404,6 +410,34 @@ def run_decode(args, inp3, local, peaks, peak_src, world):
     st = layer.read_stats()
     layer.set_profiling(False)
     del graph
+    # The decode token range: the same weights and skewed bias, T from 1 to 128
+    sweep = []
+    for T in SWEEP_T:
+        x = wl.make_inputs(w, seed=T, device="cuda", T=T, weights_from=inp3)["x"]
+        o = torch.empty_like(x)
+        for _ in range(3):
+            layer.forward(x, dinp, w.k, w.routed_scale, out=o)
+        _, _, cnt = layer.routing()
+        na = int((cnt > 0).sum().item())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layer.forward(x, dinp, w.k, w.routed_scale, out=o)
+        torch.cuda.synchronize()
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_iter)]
+        for a, b in ev2:
+            flush.zero_()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        t_ms = statistics.median([a.elapsed_time(b) for a, b in ev2])
+        nb = decode_bytes(w, T, na)
+        sweep.append({"tokens": T, "n_active_experts": na, "ms_per_step_median": round(t_ms, 4),
+                      "hbm_gbs": round(nb / (t_ms / 1e3) / 1e9, 1),
+                      "hbm_frac": round(nb / (t_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)})
+        del g
+    assert layer.sync_status() == B.MOE_OK
     layer.close()
     ms = statistics.median(times)
     nbytes = decode_bytes(w, w.T, n_active)
@@ -424,7 +458,8 @@ def run_decode(args, inp3, local, peaks, peak_src, world):
                          "frac": round(gu_gbs / hbm, 4), "peak_source": f"{peak_src} HBM copy",
                          "bytes_per_launch": gu_bytes, "avg_launch_ms": round(gu_ms, 4),
                          "traffic": None},
-            "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}}
+            "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+            "token_sweep": sweep}
 
 
 def run_dense(args, local, peaks, peak_src, world):
@@ -495,6 +530,44 @@ def run_dense(args, local, peaks, peak_src, world):
     return res
 
 
+def run_pack(args, inp, peaks, peak_src):
+    """moe_pack_experts on the GLM-5 expert weights: the HF per-expert stacks
+    (made from the workload's grouped weights by torch transposes, outside
+    the timed region) packed back into the grouped layout; the result must
+    equal the workload's weights bit for bit."""
+    from mixture_experts_transformer_sigmoid_b300 import binding as B
+    gate_up, down = inp["gate_up"], inp["down"]
+    E, d, I2 = gate_up.shape
+    I = I2 // 2
+    G = gate_up[:, :, :I].transpose(1, 2).contiguous()
+    U = gate_up[:, :, I:].transpose(1, 2).contiguous()
+    Dn = down.transpose(1, 2).contiguous()
+    gu = torch.empty_like(gate_up)
+    dp = torch.empty_like(down)
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        B.pack_experts(G, U, Dn, gate_up=gu, down_projs=dp)
+    torch.cuda.synchronize()
+    exact = bool(torch.equal(gu, gate_up) and torch.equal(dp, down))
+    n = max(3, min(args.steps, 10))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        B.pack_experts(G, U, Dn, gate_up=gu, down_projs=dp)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    nbytes = 2 * 3 * E * d * I * gate_up.element_size()   # every element read once, written once
+    gbs = nbytes / (ms / 1e3) / 1e9
+    del G, U, Dn, gu, dp
+    torch.cuda.empty_cache()
+    return {"experts": E, "hidden": d, "inter": I, "ms": round(ms, 4), "bytes": nbytes,
+            "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+            "peak_source": f"{peak_src} HBM copy", "exact": exact, "launches": 3,
+            "call": "moe_pack_experts (HF per-expert stacks -> gate_and_up_projs, down_projs)"}
+
+
 # ------------------------------------------------------------ reference arm
 def run_reference(args, world):
     """The CPU oracle on the host cores, on bounded samples of the workload."""
@@ -538,6 +611,7 @@ def main():
     ap.add_argument("--workload", default="glm5_prefill", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--no-decode", dest="decode", action="store_false")
     ap.add_argument("--no-dense", dest="dense", action="store_false")
+    ap.add_argument("--no-pack", dest="pack", action="store_false")
     ap.add_argument("--only-dense", action="store_true",
                     help="time only the dense feed-forward block (about 1 GB on the device; "
                          "the case for profiling its kernels)")

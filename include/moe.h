@@ -252,6 +252,27 @@ MOE_API moe_status moe_route_static(int32_t T, int32_t E, int32_t top_k, float r
                             int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* row_tok,
                             float* row_w, void* stream);
 
+/* Packs HF per-expert nn.Linear weights into the grouped native layout that
+ * moe_forward reads (NeMo AutoModel GLM4-MoE state dict adapter page:
+ * experts.{E}.gate_proj / up_proj / down_proj are grouped into
+ * gate_and_up_projs [n_experts, dim, 2*moe_inter_dim] and down_projs
+ * [n_experts, moe_inter_dim, dim]).  Device pointers, row-major:
+ *   gate, up [E, I, d], down [E, d, I]   the E experts' HF tensors, stacked
+ *   gate_up [E, d, 2I]   gate_up[e][j][i] = gate[e][i][j],
+ *                        gate_up[e][j][I + i] = up[e][i][j]
+ *   down_projs [E, I, d] down_projs[e][i][o] = down[e][o][i]
+ * A caller holding the experts as separate tensors calls once per expert
+ * with E = 1 and the outputs advanced by e experts.  elem_bytes is 2 (bf16)
+ * or 4 (fp32); the copy is exact.  Either output may be NULL to skip it (its
+ * inputs are then not read).  Pointers 4-byte aligned; outputs must not
+ * overlap the inputs or each other (MOE_ERR_INVALID_ARG).  E == 0 queues
+ * nothing; E > 65535, or odd d or I with 2-byte elements, give
+ * MOE_ERR_UNSUPPORTED.  No handle, no allocation; asynchronous on `stream`
+ * (the calling thread's current device). */
+MOE_API moe_status moe_pack_experts(int32_t E, int32_t d, int32_t I, int32_t elem_bytes,
+                            const void* gate, const void* up, const void* down, void* gate_up,
+                            void* down_projs, void* stream);
+
 /* Static description of a status code. */
 MOE_API const char* moe_status_string(moe_status s);
 

@@ -24,7 +24,7 @@ T_XN, T_LOGITS, T_OFFSETS, T_POS, T_ROW_TOK, T_H, T_SHARED = range(7)
 EXPORTS = ("moe_init", "moe_forward", "moe_forward_host", "moe_forward_host_async",
            "moe_forward_host_wait", "moe_dense_forward", "moe_get_routing",
            "moe_get_intermediate", "moe_sync_status", "moe_set_profiling", "moe_read_stats",
-           "moe_destroy", "moe_route_static", "moe_status_string")
+           "moe_destroy", "moe_route_static", "moe_pack_experts", "moe_status_string")
 STAGES = ("rmsnorm", "router", "topk", "scan", "scatter", "gather", "gate_up_swiglu",
           "down_weighted", "combine")
 
@@ -76,6 +76,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_read_stats.argtypes = [P, ctypes.POINTER(MoeStats)]
     lib.moe_destroy.argtypes = [P]
     lib.moe_route_static.argtypes = [I32, I32, I32, F32, P, P, P, P, P, P, P, P, P, P]
+    lib.moe_pack_experts.argtypes = [I32, I32, I32, I32, P, P, P, P, P, P]
     lib.moe_status_string.argtypes = [ctypes.c_int]
     lib.moe_status_string.restype = ctypes.c_char_p
     for name in EXPORTS[:-1]:
@@ -257,3 +258,22 @@ def route_static(logits: torch.Tensor, corr_bias: torch.Tensor, top_k: int,
                            f"static scratch limit of {ROUTE_STATIC_MAX_CELLS} cells")
     _check(st, "moe_route_static")
     return res
+
+
+def pack_experts(gate: torch.Tensor, up: torch.Tensor, down: torch.Tensor,
+                 gate_up: Optional[torch.Tensor] = None, down_projs: Optional[torch.Tensor] = None,
+                 stream=None):
+    """moe_pack_experts: HF per-expert weights (gate, up [E, I, d], down
+    [E, d, I], stacked) -> the grouped layout gate_up [E, d, 2I] and
+    down_projs [E, I, d] that MoeSublayer.forward reads."""
+    E, I, d = gate.shape
+    if gate_up is None:
+        gate_up = torch.empty((E, d, 2 * I), dtype=gate.dtype, device=gate.device)
+    if down_projs is None:
+        down_projs = torch.empty((E, I, d), dtype=down.dtype, device=down.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(gate.device)
+    _check(load_library().moe_pack_experts(E, d, I, gate.element_size(), _ptr(gate), _ptr(up), _ptr(down),
+                                           _ptr(gate_up), _ptr(down_projs),
+                                           ctypes.c_void_p(stream.cuda_stream)), "moe_pack_experts")
+    return gate_up, down_projs

@@ -28,6 +28,7 @@
 
 #include "k_gemm_pair.cuh"
 #include "k_gemm_tc.cuh"
+#include "k_pack.cuh"
 #include "k_route.cuh"
 #include "k_router_tc.cuh"
 #include "moe.h"
@@ -689,6 +690,48 @@ moe_status moe_route_static(int32_t T, int32_t E, int32_t top_k, float routed_sc
                                                                chunk_base);
     scatter_kernel<<<nch, CHUNK_TOKENS, E * (CHUNK_TOKENS / 32) * sizeof(uint32_t), st>>>(
         idx, w, T, E, top_k, chunk_base, pos, row_tok, row_w);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_pack_experts(int32_t E, int32_t d, int32_t I, int32_t elem_bytes, const void* gate,
+                            const void* up, const void* down, void* gate_up, void* down_projs,
+                            void* stream) {
+    if (E < 0 || d < 1 || I < 1 || (elem_bytes != 2 && elem_bytes != 4)) return MOE_ERR_INVALID_ARG;
+    if (E > 65535 || (elem_bytes == 2 && (d % 2 != 0 || I % 2 != 0))) return MOE_ERR_UNSUPPORTED;
+    if (E == 0 || (gate_up == nullptr && down_projs == nullptr)) return MOE_OK;
+    auto word_aligned = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+    if (gate_up != nullptr && (!word_aligned(gate) || !word_aligned(up) || !word_aligned(gate_up)))
+        return MOE_ERR_INVALID_ARG;
+    if (down_projs != nullptr && (!word_aligned(down) || !word_aligned(down_projs))) return MOE_ERR_INVALID_ARG;
+    const size_t n = static_cast<size_t>(E) * d * I * elem_bytes;   // bytes of each HF stack
+    const struct { const void* p; size_t n; } ins[] = {{gate, n}, {up, n}, {down, n}};
+    for (const auto& in : ins) {
+        if (in.p == nullptr) continue;
+        if (gate_up != nullptr && overlaps(gate_up, 2 * n, in.p, in.n)) return MOE_ERR_INVALID_ARG;
+        if (down_projs != nullptr && overlaps(down_projs, n, in.p, in.n)) return MOE_ERR_INVALID_ARG;
+    }
+    if (gate_up != nullptr && down_projs != nullptr && overlaps(gate_up, 2 * n, down_projs, n))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint64_t dI = static_cast<uint64_t>(d) * I;
+    // out[b][c][col_off + r] = in[b][r][c] over R x C inputs
+    auto launch = [&](const void* in, int R, int C, void* out, int out_ld, int col_off) {
+        const dim3 grid((C + PACK_TILE - 1) / PACK_TILE, (R + PACK_TILE - 1) / PACK_TILE, E);
+        const uint64_t out_bstride = static_cast<uint64_t>(C) * out_ld;
+        if (elem_bytes == 2)
+            pack_transpose_b16_kernel<<<grid, PACK_THREADS, 0, st>>>(
+                static_cast<const uint32_t*>(in), R, C, dI / 2, static_cast<uint32_t*>(out), out_ld, col_off,
+                out_bstride / 2);
+        else
+            pack_transpose_b32_kernel<<<grid, PACK_THREADS, 0, st>>>(
+                static_cast<const uint32_t*>(in), R, C, dI, static_cast<uint32_t*>(out), out_ld, col_off,
+                out_bstride);
+    };
+    if (gate_up != nullptr) {
+        launch(gate, I, d, gate_up, 2 * I, 0);   // gate_and_up[e][j][i]     = gate[e][i][j]
+        launch(up, I, d, gate_up, 2 * I, I);     // gate_and_up[e][j][I + i] = up[e][i][j]
+    }
+    if (down_projs != nullptr) launch(down, d, I, down_projs, d, 0);   // down_projs[e][i][o] = down[e][o][i]
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -2,9 +2,15 @@
 run the CUDA path through the C ABI and compare it with the CPU oracle.
 
 Tolerances (floating point):
-  bf16 storage: max|gpu - oracle| <= 2e-2 * rms(oracle) and
+  bf16 storage: |gpu - oracle| <= 2e-2 * rms(oracle) + half a bf16 ulp of the
+                oracle value, elementwise, and
                 sum|gpu - oracle| / sum|oracle| <= 5e-3
   fp32 storage: max|gpu - oracle| <= 1e-4 * rms(oracle)
+The half ulp is the output's own rounding to bf16 (up to 2^-8 |out|), which
+the stored dtype makes unavoidable: on its own it exceeds 2e-2 * rms(oracle)
+wherever |out| > 5.12 rms(oracle), and the tail of a few hundred thousand
+outputs reaches that range.  The plain max|gpu - oracle| / rms(oracle) is
+reported beside it.
 Routing: expert ids are compared exactly; a token may differ only when its
 top-k margin b_(k) - b_(k+1) is below 1e-5 (several selections are then
 correct) or when its RMSNorm output differs in some bf16 rounding from the
@@ -158,6 +164,21 @@ def output_errors(gpu, ref):
             "mean_rel": float(diff.sum() / max(np.abs(ref).sum(), 1e-30))}
 
 
+def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 values (8 significant bits) around |v|."""
+    a = np.abs(v.astype(np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.where(a > 0, 2.0 ** (e - 8), 0.0)
+
+
+def check_bf16_max(gpu, ref, max_rms):
+    """Elementwise |gpu - ref| <= max_rms * rms(ref) + half_ulp_bf16(ref)."""
+    ref64 = ref.astype(np.float64)
+    rms = float(np.sqrt(np.mean(ref64 ** 2)))
+    excess = np.abs(gpu.astype(np.float64) - ref64) - (max_rms * rms + half_ulp_bf16(ref64))
+    assert excess.max(initial=-1.0) <= 0.0, f"bf16 output error above the bound by {float(excess.max())}"
+
+
 def check_output(g, host, c, dtype, rows=None):
     """Oracle on the GPU's selection for the given rows; returns error stats
     of the output and of the MoE delta (out - x)."""
@@ -169,9 +190,11 @@ def check_output(g, host, c, dtype, rows=None):
     x = (x.astype(np.uint32) << 16).view(np.float32) if x.dtype == np.uint16 else x
     sd = output_errors(gout - x, r["out"] - x)
     tol = TOL[dtype]
-    assert st["max_over_rms"] <= tol["max_rms"], st
     if dtype == "bf16":
+        check_bf16_max(gout, r["out"], tol["max_rms"])
         assert st["mean_rel"] <= tol["mean_rel"], st
+    else:
+        assert st["max_over_rms"] <= tol["max_rms"], st
     return {"out": st, "delta": sd}
 
 

@@ -145,3 +145,32 @@ def test_host_io_entry_points_reject_a_null_handle(lib):
     nulls = [None] * 11
     assert lib.moe_forward_host_async(None, 4, *nulls[:9], 2, 1.0, None, None) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_forward_host_wait(None) == B.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("E,d,I,eb,status", [
+    (-1, 64, 64, 2, B.MOE_ERR_INVALID_ARG), (2, 0, 64, 2, B.MOE_ERR_INVALID_ARG),
+    (2, 64, 0, 2, B.MOE_ERR_INVALID_ARG), (2, 64, 64, 3, B.MOE_ERR_INVALID_ARG),
+    (70000, 64, 64, 2, B.MOE_ERR_UNSUPPORTED),           # grid z limit
+    (2, 63, 64, 2, B.MOE_ERR_UNSUPPORTED),               # bf16 moves whole 4-byte words
+    (2, 64, 65, 2, B.MOE_ERR_UNSUPPORTED),
+    (0, 64, 64, 2, B.MOE_OK),                            # nothing to do, no pointer read
+])
+def test_pack_experts_host_checks(lib, E, d, I, eb, status):
+    p = [ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), ctypes.c_void_p(3 << 20)]
+    out = [ctypes.c_void_p(8 << 20), ctypes.c_void_p(16 << 20)]
+    assert lib.moe_pack_experts(E, d, I, eb, *p, *out, None) == status
+
+
+def test_pack_experts_pointer_checks(lib):
+    g, u, dn = ctypes.c_void_p(1 << 24), ctypes.c_void_p(2 << 24), ctypes.c_void_p(3 << 24)
+    gu, do = ctypes.c_void_p(4 << 24), ctypes.c_void_p(6 << 24)
+    E, d, I = 2, 64, 64       # each HF stack is 16 KB, gate_up 32 KB
+    assert lib.moe_pack_experts(E, d, I, 2, g, u, dn, None, None, None) == B.MOE_OK  # no outputs
+    assert lib.moe_pack_experts(E, d, I, 2, None, u, dn, gu, None, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_pack_experts(E, d, I, 2, g, u, None, None, do, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_pack_experts(E, d, I, 2, ctypes.c_void_p((1 << 24) + 2), u, dn, gu, None,
+                                None) == B.MOE_ERR_INVALID_ARG                   # misaligned
+    assert lib.moe_pack_experts(E, d, I, 2, g, u, dn, ctypes.c_void_p((2 << 24) + 64), None,
+                                None) == B.MOE_ERR_INVALID_ARG                   # output over `up`
+    assert lib.moe_pack_experts(E, d, I, 2, g, u, dn, gu, ctypes.c_void_p((4 << 24) + 1024),
+                                None) == B.MOE_ERR_INVALID_ARG                   # outputs overlap

@@ -6,7 +6,8 @@ layer excerpt on the GLM-5 shared-expert page).
 Small cases compare every token on both GEMM paths (single-CTA tiles below
 128 tokens, CTA pairs from 128 up) and the CUDA-core path; the GLM-5-sized
 cases compare a seeded sample of tokens.  The output is held to the
-sublayer's tolerances (tests/parity.py).  The MLP's own contribution
+sublayer's tolerances (tests/parity.py, with its half-ulp allowance for the
+output's own rounding to bf16).  The MLP's own contribution
 out - x is checked too: in fp32 to 1e-4 of its rms; in bf16 elementwise to
 2^-8 |out| (the worst case of the one rounding of out to bf16, which is
 relative to |out|, not to the contribution) plus 2e-2 of its rms.  With the
@@ -77,9 +78,12 @@ def compare(w, gout, host, rows):
     st = parity.output_errors(g, ref)
     sd = parity.output_errors(g - x, ref - x)
     tol = parity.TOL[w.dtype]
-    assert st["max_over_rms"] <= tol["max_rms"], (st, sd)
     if w.dtype == "bf16":
+        parity.check_bf16_max(g, ref, tol["max_rms"])
         assert st["mean_rel"] <= tol["mean_rel"], (st, sd)
+    else:
+        assert st["max_over_rms"] <= tol["max_rms"], (st, sd)
+    if w.dtype == "bf16":
         rms_delta = float(np.sqrt(np.mean((ref - x) ** 2)))
         bound = 2.0 ** -8 * np.abs(ref) + 2e-2 * rms_delta
         excess = np.abs(g - ref) - bound

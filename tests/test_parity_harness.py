@@ -2,6 +2,7 @@
 'device' result, every check passes; given a planted error, the checks fail."""
 import numpy as np
 import pytest
+import torch
 
 import parity
 from mixture_experts_transformer_sigmoid_b300 import workloads as wl
@@ -68,3 +69,26 @@ def test_slot_order_may_swap_only_near_tied_experts():
     assert not set_diff.any() and order_bad.all()          # 0.5 placed before 0.9
     set_diff, _ = parity.selection_diff(np.array([[0, 1, 3]]), oracle_sel, b)
     assert set_diff.all()
+
+
+def test_half_ulp_bounds_bf16_rounding_and_is_reached():
+    rng = np.random.default_rng(3)
+    v = (rng.standard_normal(100000) * np.exp(rng.uniform(-20, 20, 100000))).astype(np.float32)
+    r = torch.from_numpy(v).to(torch.bfloat16).float().numpy()
+    err = np.abs(r.astype(np.float64) - v.astype(np.float64))
+    assert np.all(err <= parity.half_ulp_bf16(v))
+    # a tie: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 and rounds to even (1)
+    t = np.array([1.0 + 2.0 ** -8], np.float32)
+    rt = torch.from_numpy(t).to(torch.bfloat16).float().numpy()
+    assert abs(float(rt[0]) - float(t[0])) == parity.half_ulp_bf16(t)[0] == 2.0 ** -8
+
+
+def test_bf16_max_check_allows_rounding_and_catches_more():
+    rng = np.random.default_rng(4)
+    ref = (rng.standard_normal(200000) * 1.7).astype(np.float32)
+    rounded = torch.from_numpy(ref).to(torch.bfloat16).float().numpy()
+    parity.check_bf16_max(rounded, ref, 2e-2)            # the exact result, stored in bf16
+    bad = rounded.copy()
+    bad[123] += 0.05 * 1.7                               # 5e-2 rms off in one element
+    with pytest.raises(AssertionError):
+        parity.check_bf16_max(bad, ref, 2e-2)
