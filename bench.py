@@ -523,7 +523,8 @@ def run_dense(args, local, peaks, peak_src, world):
                 "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
                 "peak_source": f"{peak_src} HBM copy",
                 "l2": "256 MB buffer written between steps (outside the timed events)",
-                "launch": "CUDA graph replay of one moe_dense_forward (3 kernels)"}
+                "launch": "CUDA graph replay of one moe_dense_forward (4 kernels: the down "
+                          "projection split over k-ranges, then their fixed-order sum)"}
         assert layer.sync_status() == B.MOE_OK
         del graph
     layer.close()

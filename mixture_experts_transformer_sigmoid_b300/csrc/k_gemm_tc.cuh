@@ -49,7 +49,9 @@ constexpr int DEVERR_TIMEOUT = 1;
 // SWIGLU: out = silu(gate) * up, from the gate and up halves of the A rows.
 // WEIGHTED: out = row_w[row] * acc (row_w null: acc).
 // RESIDUAL: out = res[row, col] + acc, added in fp32 and rounded once.
-enum EpiKind { EPI_SWIGLU = 1, EPI_WEIGHTED = 2, EPI_RESIDUAL = 3 };
+// PARTIAL: fp32 acc of one k-range of a split dense segment, to
+//   out[k-range][row][col] (single-CTA kernel; the ranges are added later).
+enum EpiKind { EPI_SWIGLU = 1, EPI_WEIGHTED = 2, EPI_RESIDUAL = 3, EPI_PARTIAL = 4 };
 
 struct TcSeg {
     int grouped;          // 1: expert groups from offsets[]; 0: one group of n_rows rows
@@ -66,6 +68,7 @@ struct TcSeg {
     int a_kind;           // CTA-pair kernel: how a0 delivers the 128 A rows (PairAKind)
     const void* res;      // residual epilogue: bf16 [rows, ld_out], indexed like out
     int f_group;          // dense segment: feature tiles per tile group (0: all of them)
+    int k_split;          // dense segment, single-CTA kernel: k-ranges per tile (0 or 1: none)
 };
 
 struct TcParams {
@@ -82,6 +85,7 @@ struct TcParams {
 
 struct TileInfo {
     int seg, grp, row0, rows, ftile;
+    int ks, kb0, nkb;     // k-range of the tile: its index and k-blocks [kb0, kb0 + nkb)
 };
 
 // Linear tile id -> (segment, group, first row, rows, feature tile).  Tiles
@@ -95,13 +99,23 @@ struct TileInfo {
 // run together then share a few weight tiles and a few token tiles, and each
 // group's weights are read from DRAM once (token tile-major over all feature
 // tiles would stream every weight once per token tile).
+// A split dense segment (k_split > 1) repeats its tiles once per k-range,
+// k-range-major; the ranges split the k-blocks evenly.
 __device__ __forceinline__ bool decode_tile(const TcParams& p, const int* prefix, int L, int BN,
                                             TileInfo& ti) {
     for (int s = 0; s < p.n_segs; ++s) {
         const TcSeg& sg = p.seg[s];
         const int ntok = sg.grouped ? prefix[p.E] : (sg.n_rows + BN - 1) / BN;
-        const int cnt = ntok * sg.n_ftiles;
+        const int nsplit = (!sg.grouped && sg.k_split > 1) ? sg.k_split : 1;
+        const int per_split = ntok * sg.n_ftiles;
+        const int cnt = per_split * nsplit;
         if (L < cnt) {
+            const int ks = L / per_split;
+            L -= ks * per_split;
+            const int nkb_all = sg.K / TC_BK;
+            ti.ks = ks;
+            ti.kb0 = static_cast<int>(static_cast<int64_t>(ks) * nkb_all / nsplit);
+            ti.nkb = static_cast<int>(static_cast<int64_t>(ks + 1) * nkb_all / nsplit) - ti.kb0;
             int tt = L / sg.n_ftiles;
             ti.ftile = L - tt * sg.n_ftiles;
             ti.seg = s;
@@ -240,8 +254,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 const CUtensorMap* mb = &p.b[ti.seg];
                 const int nb = (ti.rows + 63) >> 6;
                 const int f0 = ti.ftile * sg.a_fstride;
-                const int nkb = sg.K / TC_BK;
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = ti.kb0; kb < ti.kb0 + ti.nkb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, TC_TIMEOUT_NS)) {
                         ok = false;
                         break;
@@ -298,8 +311,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                const int nkb = sg.K / TC_BK;
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = 0; kb < ti.nkb; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, TC_TIMEOUT_NS)) {
                         ok = false;
                         break;
@@ -387,6 +399,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                             const float wv = sg.row_w ? sg.row_w[row] : 1.0f;
                             out[static_cast<size_t>(row) * sg.ld_out + col] =
                                 __float2bfloat16_rn(__uint_as_float(v[c]) * wv);
+                        }
+                    }
+                } else if constexpr (EPI == EPI_PARTIAL) {
+                    const int col = ti.ftile * sg.a_fstride + q * 32 + lane;
+                    float* part = static_cast<float*>(sg.out) +
+                                  static_cast<size_t>(ti.ks) * sg.n_rows * sg.ld_out;
+                    if (col < sg.F) {
+                        const int cmax = min(32, ti.rows - c0);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            if (c >= cmax) break;
+                            part[static_cast<size_t>(ti.row0 + c0 + c) * sg.ld_out + col] = __uint_as_float(v[c]);
                         }
                     }
                 } else if constexpr (EPI == EPI_RESIDUAL) {

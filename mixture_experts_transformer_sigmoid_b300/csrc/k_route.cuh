@@ -602,6 +602,29 @@ __global__ void combine_kernel(const T* __restrict__ x, const T* __restrict__ sh
     }
 }
 
+// Split-K dense down projection: out = res + sum over the k-ranges of the fp32
+// partials part[s][i] (s in order, then the residual), rounded once.  n (the
+// element count) is a multiple of 4; part, res and out are 16-byte aligned.
+template <typename T>
+__global__ void splitk_residual_kernel(const float* __restrict__ part, int nsplit, size_t stride,
+                                       const T* __restrict__ res, T* __restrict__ out, size_t n) {
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n / 4;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        float4 acc = reinterpret_cast<const float4*>(part)[i];
+        for (int sp = 1; sp < nsplit; ++sp) {
+            const float4 v = reinterpret_cast<const float4*>(part + sp * stride)[i];
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        float r[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) r[j] = Elem<T>::to_f(res[4 * i + j]);
+        out[4 * i + 0] = Elem<T>::from_f(acc.x + r[0]);
+        out[4 * i + 1] = Elem<T>::from_f(acc.y + r[1]);
+        out[4 * i + 2] = Elem<T>::from_f(acc.z + r[2]);
+        out[4 * i + 3] = Elem<T>::from_f(acc.w + r[3]);
+    }
+}
+
 // ------------------------------------------------- FFMA expert kernels (fp32)
 // Expert of a permuted row: the last e with offsets[e] <= row.
 __device__ __forceinline__ int expert_of_row(const int* offsets, int E, int row) {

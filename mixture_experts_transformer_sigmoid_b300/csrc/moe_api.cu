@@ -61,6 +61,7 @@ struct moe_handle {
     void* hs = nullptr;
     void* sh = nullptr;
     void* hd = nullptr;       // dense block activations [max_tokens, dense_inter]
+    float* dpart = nullptr;   // split-K partials of the dense down projection [DENSE_SPLIT_MAX][DENSE_SPLIT_MAX_T][d]
     void* x_stage = nullptr;
     void* out_stage = nullptr;
     // pipelined host I/O (moe_forward_host_async): a second staging slot, copy
@@ -157,8 +158,8 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 void free_ws(moe_handle* h) {
     void* ptrs[] = {h->xn, h->logits, h->part, h->topk_idx, h->topk_w, h->chunk_cnt, h->chunk_base,
                     h->counts, h->offsets, h->pos, h->row_tok, h->row_w, h->xp, h->h, h->yp,
-                    h->hs, h->sh, h->hd, h->x_stage, h->out_stage, h->x_stage2, h->out_stage2,
-                    h->err};
+                    h->hs, h->sh, h->hd, h->dpart, h->x_stage, h->out_stage, h->x_stage2,
+                    h->out_stage2, h->err};
     for (void* p : ptrs)
         if (p) cudaFree(p);
 }
@@ -208,7 +209,7 @@ int tile_bound(const TcParams& prm, int BN, int P) {
         const TcSeg& sg = prm.seg[s];
         const int64_t ntok = sg.grouped ? (static_cast<int64_t>(P) + BN - 1) / BN + prm.E
                                         : (static_cast<int64_t>(sg.n_rows) + BN - 1) / BN;
-        n += ntok * sg.n_ftiles;
+        n += ntok * sg.n_ftiles * (!sg.grouped && sg.k_split > 1 ? sg.k_split : 1);
     }
     return static_cast<int>(std::min<int64_t>(n, 1 << 30));
 }
@@ -219,6 +220,20 @@ int tile_bound(const TcParams& prm, int BN, int P) {
 #ifndef MOE_DENSE_GROUP_MB
 #define MOE_DENSE_GROUP_MB 48
 #endif
+// Split-K of the dense down projection for decode-sized batches on the
+// single-CTA kernel: with T <= DENSE_SPLIT_MAX_T tokens it has only
+// ceil(T / 64) * ceil(d / 128) tiles (48 at d = 6144), too few to stream its
+// weights with every SM; up to DENSE_SPLIT_MAX k-ranges bring the tile count
+// near the SM count.
+constexpr int DENSE_SPLIT_MAX = 8;
+constexpr int DENSE_SPLIT_MAX_T = 128;
+
+int dense_down_split(int Tn, int d, int Id, int num_sms) {
+    if (Tn > DENSE_SPLIT_MAX_T) return 1;
+    const int tiles = ((Tn + 63) / 64) * ((d + 127) / 128);
+    return std::max(1, std::min({Id / 64, DENSE_SPLIT_MAX, num_sms / tiles}));
+}
+
 void set_dense_groups(TcSeg& sg, int weight_rows_per_ftile) {
     const double ftile_bytes = 2.0 * weight_rows_per_ftile * sg.K;
     if (ftile_bytes * sg.n_ftiles <= 64.0 * (1 << 20)) {
@@ -551,8 +566,22 @@ moe_status dense_impl(moe_handle* h, int Tn, const void* x_, const void* norm_w,
             g2.seg[0] = TcSeg{0, Tn, Id, 128, 64, (d + 127) / 128, d, d, out, nullptr, 0, 0, x};
             set_dense_groups(g2.seg[0], 128);
         }
-        if (run_tc<EPI_RESIDUAL>(g2, pair, Tn, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
-        h->launches += 3;
+        const int ks = pair ? 1 : dense_down_split(Tn, d, Id, h->num_sms);
+        if (ks > 1) {
+            // k-ranges of fp32 partials [ks][Tn][d], then their sum in order plus the residual
+            g2.seg[0].out = h->dpart;
+            g2.seg[0].res = nullptr;
+            g2.seg[0].k_split = ks;
+            const int grid = std::max(1, std::min(h->num_sms, tile_bound(g2, 64, Tn)));
+            if (launch_tc<64, 8, EPI_PARTIAL>(g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+            const size_t n = static_cast<size_t>(Tn) * d;
+            splitk_residual_kernel<T><<<static_cast<int>(std::min<size_t>((n / 4 + 255) / 256, 4 * h->num_sms)), 256,
+                                        0, st>>>(h->dpart, ks, n, x, static_cast<T*>(out), n);
+            h->launches += 4;
+        } else {
+            if (run_tc<EPI_RESIDUAL>(g2, pair, Tn, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+            h->launches += 3;
+        }
     } else {
         simt_shared_gate_up_kernel<T><<<dim3(Tn, (Id + 127) / 128), 128, d * sizeof(float), st>>>(
             xn, static_cast<const T*>(gw), static_cast<const T*>(uw), d, Id, hd);
@@ -817,7 +846,10 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out) {
     alloc(&h->yp, P * d * es);
     alloc(&h->hs, T * std::max<size_t>(Is, 1) * es);
     alloc(&h->sh, T * d * es);
-    if (c.dense_inter > 0) alloc(&h->hd, T * static_cast<size_t>(c.dense_inter) * es);
+    if (c.dense_inter > 0) {
+        alloc(&h->hd, T * static_cast<size_t>(c.dense_inter) * es);
+        if (tc) alloc(&h->dpart, static_cast<size_t>(DENSE_SPLIT_MAX) * std::min<size_t>(T, DENSE_SPLIT_MAX_T) * d * 4);
+    }
     if (!dense_only) {   // host-I/O staging of moe_forward_host(_async)
         alloc(&h->x_stage, T * d * es);
         alloc(&h->out_stage, T * d * es);

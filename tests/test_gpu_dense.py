@@ -4,7 +4,8 @@ first first_k_dense_replace decoder layers use instead of the MoE (decoder
 layer excerpt on the GLM-5 shared-expert page).
 
 Small cases compare every token on both GEMM paths (single-CTA tiles below
-128 tokens, CTA pairs from 128 up) and the CUDA-core path; the GLM-5-sized
+128 tokens, with the down projection split over k-ranges; CTA pairs from 128
+up) and the CUDA-core path; the GLM-5-sized
 cases compare a seeded sample of tokens.  The output is held to the
 sublayer's tolerances (tests/parity.py, with its half-ulp allowance for the
 output's own rounding to bf16).  The MLP's own contribution
@@ -179,8 +180,9 @@ def test_dense_on_a_moe_handle_leaves_the_moe_results_alone():
     np.testing.assert_array_equal(parity.to_np_f32(d1), run_dense(wd, di))
 
 
-def test_dense_graph_replay_matches_direct_call():
-    w = SMALL["dense_pair_odd_bf16"]
+@pytest.mark.parametrize("name", ["dense_pair_odd_bf16", "dense_single_odd_bf16"])  # CTA pairs / split-K
+def test_dense_graph_replay_matches_direct_call(name):
+    w = SMALL[name]
     dev = {k: v.cuda() for k, v in wl.make_dense_inputs(w).items()}
     layer = dense_layer(w)
     try:
