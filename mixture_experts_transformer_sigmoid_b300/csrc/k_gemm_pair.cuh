@@ -57,7 +57,9 @@ enum PairAKind {
 };
 
 // Position of a CTA's producer in its sequence of (tile, k-block) loads, with
-// the coordinates of the CTA's half of the tile.
+// the coordinates of the CTA's half of the tile.  Every tile runs over its
+// segment's whole K: segments given to this kernel are never split over
+// k-ranges (TcSeg::k_split is for the single-CTA kernel).
 struct PairCursor {
     int L, kb, nkb;
     int f0;      // first feature of this CTA's A rows
