@@ -191,6 +191,15 @@ MOE_API moe_status moe_get_intermediate(moe_handle* h, moe_tensor which, void* d
  * call, MOE_ERR_CUDA on an asynchronous CUDA error, else MOE_OK. */
 MOE_API moe_status moe_sync_status(moe_handle* h, void* stream);
 
+/* Self-test of failure detection (no counterpart in the paper): queues on
+ * `stream` one wait on a device barrier that nothing completes, bounded like
+ * every wait of the library's tensor-core kernels.  After timeout_us
+ * microseconds (1 .. 1,000,000) the wait gives up and sets the handle's
+ * device error flag, so the next moe_sync_status returns MOE_ERR_TIMEOUT and
+ * clears it.  Nothing faults or hangs, and the context stays usable: it is
+ * the path a kernel takes when a copy or a peer never arrives. */
+MOE_API moe_status moe_selftest_wait_timeout(moe_handle* h, uint32_t timeout_us, void* stream);
+
 /* Counters of the forwards run since the last moe_read_stats. */
 #define MOE_MAX_STAGES 16
 typedef struct {

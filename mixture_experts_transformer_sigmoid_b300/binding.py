@@ -23,7 +23,8 @@ T_XN, T_LOGITS, T_OFFSETS, T_POS, T_ROW_TOK, T_H, T_SHARED = range(7)
 # Functions the header declares (kept in sync by the ABI test).
 EXPORTS = ("moe_init", "moe_forward", "moe_forward_host", "moe_forward_host_async",
            "moe_forward_host_wait", "moe_dense_forward", "moe_get_routing",
-           "moe_get_intermediate", "moe_sync_status", "moe_set_profiling", "moe_read_stats",
+           "moe_get_intermediate", "moe_sync_status", "moe_selftest_wait_timeout",
+           "moe_set_profiling", "moe_read_stats",
            "moe_destroy", "moe_route_static", "moe_pack_experts", "moe_status_string")
 STAGES = ("rmsnorm", "router", "topk", "scan", "scatter", "gather", "gate_up_swiglu",
           "down_weighted", "combine")
@@ -72,6 +73,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_get_routing.argtypes = [P, P, P, P, P]
     lib.moe_get_intermediate.argtypes = [P, ctypes.c_int, P, ctypes.c_size_t, P]
     lib.moe_sync_status.argtypes = [P, P]
+    lib.moe_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P]
     lib.moe_set_profiling.argtypes = [P, I32]
     lib.moe_read_stats.argtypes = [P, ctypes.POINTER(MoeStats)]
     lib.moe_destroy.argtypes = [P]
@@ -212,6 +214,12 @@ class MoeSublayer:
 
     def sync_status(self, stream=None) -> int:
         return self.lib.moe_sync_status(self.handle, self._stream(stream))
+
+    def selftest_wait_timeout(self, timeout_us: int, stream=None):
+        """Queues a bounded wait that nothing completes; the next
+        sync_status reports MOE_ERR_TIMEOUT."""
+        _check(self.lib.moe_selftest_wait_timeout(self.handle, timeout_us, self._stream(stream)),
+               "moe_selftest_wait_timeout")
 
     def set_profiling(self, enable: bool):
         _check(self.lib.moe_set_profiling(self.handle, 1 if enable else 0), "moe_set_profiling")

@@ -441,4 +441,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     if (threadIdx.x == 0 && *abort_flag) atomicOr(p.err, DEVERR_TIMEOUT);
 }
 
+// Self-test of the bounded waits above: one thread waits on an mbarrier that
+// nothing arrives at, with the same wait helper, gives up after timeout_ns
+// as a kernel whose producer or peer stalled would, and sets the device
+// error flag.  Nothing faults and nothing hangs.
+__global__ void wait_timeout_selftest_kernel(int* err, uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    __shared__ volatile int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+    if (!mbar_wait(&bar, 0, &abort_flag, timeout_ns)) atomicOr(err, DEVERR_TIMEOUT);
+}
+
 }  // namespace moe

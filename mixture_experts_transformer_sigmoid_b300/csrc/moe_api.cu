@@ -1043,6 +1043,14 @@ moe_status moe_sync_status(moe_handle* h, void* stream) {
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+moe_status moe_selftest_wait_timeout(moe_handle* h, uint32_t timeout_us, void* stream) {
+    if (!h || timeout_us < 1 || timeout_us > 1000000) return MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+    wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        h->err, static_cast<uint64_t>(timeout_us) * 1000u);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 moe_status moe_set_profiling(moe_handle* h, int32_t enable) {
     if (!h) return MOE_ERR_INVALID_ARG;
     if (cudaSetDevice(h->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;

@@ -115,6 +115,7 @@ def test_calls_on_null_handle(lib):
     assert lib.moe_get_intermediate(None, 0, p, 16, None) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_sync_status(None, None) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_dense_forward(None, 1, p, p, p, p, p, 64, p, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_wait_timeout(None, 1000, None) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_destroy(None) == B.MOE_OK
 
 
