@@ -39,6 +39,20 @@ static inline float round_bf16(float f) {
     return f;
 }
 
+/* Round a real value (given in fp64) to the nearest bf16 value, ties to even:
+ * one rounding of the exact value, not two (fp64 -> fp32 -> bf16 could round
+ * twice).  bf16 has fp32's exponent range and 8 significant bits. */
+static inline float round_bf16_exact(double v) {
+    if (v == 0.0 || !isfinite(v)) return (float)v;
+    int e;
+    frexp(v, &e);                                   /* |v| in [2^(e-1), 2^e) */
+    double q = ldexp(1.0, e - 8);                   /* bf16 spacing in that binade */
+    if (q < ldexp(1.0, -133)) q = ldexp(1.0, -133); /* subnormal range: fixed spacing */
+    double m = v / q;                               /* exact: a power-of-two scaling */
+    double r = nearbyint(m);                        /* ties to even in the default mode */
+    return (float)(r * q);
+}
+
 static inline double silu(double z) { return z / (1.0 + exp(-z)); }
 
 /* ---- step A: RMSNorm (GlmMoeDsaRMSNorm.forward) --------------------------- */
@@ -324,6 +338,60 @@ int oracle_dense_forward(const oracle_cfg* c, int64_t n, const int64_t* rows, co
             }
         }
         free(xn); free(acc); free(h);
+    }
+    return failed ? 2 : 0;
+}
+
+/* The query compression of GLM-5's sparse latent attention (GLM-5 "Query
+ * latent" page, MLA __init__ and the query lines of its forward):
+ *   c = q_a_proj(hidden)      nn.Linear(d -> rank, no bias, attention_bias is
+ *                             false), its output in the input precision;
+ *   q = q_a_layernorm(c)      GlmMoeDsaRMSNorm(rank), eps = c->eps (the page's
+ *                             latent RMSNorms take the 1e-6 default).
+ * w_qa is [rank, d] (nn.Linear [out, in]), gain [rank].  The Linear's output is
+ * the exact sum rounded once to the storage dtype (bf16 or fp32); the RMSNorm
+ * is step A's (rmsnorm_row) over the rank values of c.  c_out and q_out are
+ * [n, rank] fp32 values (bf16-representable for dtype 1); c_out may be NULL. */
+int oracle_q_latent(const oracle_cfg* c, int32_t rank, int64_t n, const int64_t* rows,
+                    const void* hidden, const void* w_qa, const void* gain, float* c_out,
+                    float* q_out) {
+    if (!c || !hidden || !w_qa || !gain || !q_out || n < 0 || c->d < 1 || rank < 1) return 1;
+    const int d = c->d;
+    oracle_cfg cr = *c;       /* the norm runs over the rank features of c */
+    cr.d = rank;
+    int failed = 0;
+#pragma omp parallel
+    {
+        float* cq = (float*)malloc(sizeof(float) * rank);
+        uint16_t* cq16 = (uint16_t*)malloc(sizeof(uint16_t) * rank);
+        if (!cq || !cq16) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t t = 0; t < n; ++t) {
+                int64_t row = rows ? rows[t] : t;
+                for (int r = 0; r < rank; ++r) {
+                    double acc = 0.0;
+                    for (int j = 0; j < d; ++j)
+                        acc += (double)get(hidden, row * d + j, c->dtype) *
+                               (double)get(w_qa, (int64_t)r * d + j, c->dtype);
+                    cq[r] = c->dtype == 1 ? round_bf16_exact(acc) : (float)acc;
+                }
+                const void* cin = cq;
+                if (c->dtype == 1) {          /* rmsnorm_row reads storage: bf16 bit patterns */
+                    for (int r = 0; r < rank; ++r) {
+                        uint32_t u;
+                        memcpy(&u, &cq[r], sizeof u);
+                        cq16[r] = (uint16_t)(u >> 16);
+                    }
+                    cin = cq16;
+                }
+                rmsnorm_row(&cr, cin, 0, gain, q_out + t * rank);
+                if (c_out) memcpy(c_out + t * rank, cq, sizeof(float) * rank);
+            }
+        }
+        free(cq); free(cq16);
     }
     return failed ? 2 : 0;
 }

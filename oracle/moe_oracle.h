@@ -23,7 +23,8 @@
  *      sh = Ds @ (silu(Gs @ xn) * (Us @ xn))
  *   I  out = x + sh + sum_j w_j * y_j   (GlmMoeDsaDecoderLayer.forward,
  *      second residual add)
- * and, for the dense layers, out = x + GlmMoeDsaMLP(xn) (oracle_dense_forward).
+ * and, for the dense layers, out = x + GlmMoeDsaMLP(xn) (oracle_dense_forward), and
+ * the query compression of the attention (oracle_q_latent: q_a_layernorm(q_a_proj(h))).
  *
  * Precision: inputs are read exactly (bf16 bit patterns widened to fp32);
  * sums run in fp64 and are rounded to fp32 at the step boundaries above.
@@ -85,6 +86,15 @@ int oracle_forward(const oracle_cfg* c, int64_t n, const int64_t* rows,
 int oracle_dense_forward(const oracle_cfg* c, int64_t n, const int64_t* rows, const void* x,
                          const void* gain, const void* gate, const void* up, const void* down,
                          float* out, float* xn);
+
+/* The query compression of GLM-5's sparse latent attention: c = q_a_proj(hidden)
+ * (nn.Linear d -> rank, no bias, w_qa [rank, d], the exact sum rounded once to
+ * the storage dtype) and q = q_a_layernorm(c) (step A over the rank values of
+ * c, gain [rank], eps = c->eps), for the rows listed in `rows` (NULL = rows
+ * 0..n-1 of hidden [*, d]).  c_out (may be NULL) and q_out are [n, rank] fp32. */
+int oracle_q_latent(const oracle_cfg* c, int32_t rank, int64_t n, const int64_t* rows,
+                    const void* hidden, const void* w_qa, const void* gain, float* c_out,
+                    float* q_out);
 
 /* Number of learned values and buffers the sublayer reads, RMSNorm gain excluded:
  * E*d*2I + E*I*d + 3*d*Is + E*d + E. */

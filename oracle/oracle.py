@@ -58,11 +58,13 @@ def load():
                                        P, P, P, P, P, P]
         lib.oracle_dense_forward.argtypes = [ctypes.POINTER(OracleCfg), ctypes.c_int64, P,
                                              P, P, P, P, P, P, P]
+        lib.oracle_q_latent.argtypes = [ctypes.POINTER(OracleCfg), ctypes.c_int32, ctypes.c_int64,
+                                        P, P, P, P, P, P]
         lib.oracle_param_count.argtypes = [ctypes.POINTER(OracleCfg)]
         lib.oracle_param_count.restype = ctypes.c_int64
         lib.oracle_num_threads.restype = ctypes.c_int
         for f in (lib.oracle_rmsnorm, lib.oracle_route, lib.oracle_select, lib.oracle_forward,
-                  lib.oracle_dense_forward):
+                  lib.oracle_dense_forward, lib.oracle_q_latent):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -174,6 +176,25 @@ def dense_forward(c: OracleCfg, a: dict, rows: Optional[np.ndarray] = None):
         _ptr(res["out"]), _ptr(res["xn"]))
     assert rc == 0, rc
     return res
+
+
+def q_latent(d: int, rank: int, dtype, hidden: np.ndarray, w_qa: np.ndarray, gain: np.ndarray,
+             eps: float = 1e-6, rows: Optional[np.ndarray] = None):
+    """The query compression of GLM-5's sparse latent attention (GLM-5 "Query
+    latent" page: q_resid = q_a_layernorm(q_a_proj(hidden_states)), q_a_proj
+    an nn.Linear(d -> rank) without bias, q_a_layernorm a GlmMoeDsaRMSNorm(rank)).
+    hidden [n, d], w_qa [rank, d] and gain [rank] as stored.  Returns (c, q):
+    the query latent before and after the norm, [n, rank] fp32 values."""
+    c = cfg(d, 1, 1, 0, 1, dtype, eps)
+    _check_storage(c, hidden, w_qa, gain)
+    n = hidden.shape[0] if rows is None else len(rows)
+    rows_arr = None if rows is None else np.ascontiguousarray(rows, np.int64)
+    c_out = np.empty((n, rank), np.float32)
+    q_out = np.empty((n, rank), np.float32)
+    rc = load().oracle_q_latent(ctypes.byref(c), rank, n, _ptr(rows_arr), _ptr(hidden), _ptr(w_qa),
+                                _ptr(gain), _ptr(c_out), _ptr(q_out))
+    assert rc == 0, rc
+    return c_out, q_out
 
 
 def pack_experts(gate: np.ndarray, up: np.ndarray, down: np.ndarray):

@@ -496,3 +496,68 @@ def test_packing_is_exact_data_movement():
             for i in range(I):
                 assert gate_up[e, j, i] == G[e, i, j] and gate_up[e, j, I + i] == U[e, i, j]
                 assert down[e, i, j] == Dn[e, j, i]
+
+
+# ---------------------------------------------------------------------------
+# Query compression of the sparse latent attention (GLM-5 "Query latent" page:
+# q_resid = q_a_layernorm(q_a_proj(hidden_states)), q_a_proj = nn.Linear(d ->
+# q_lora_rank, no bias), q_a_layernorm = GlmMoeDsaRMSNorm(q_lora_rank)).
+# ---------------------------------------------------------------------------
+def torch_rmsnorm_bf16(cq, gain, eps):
+    """The RMSNorm excerpt's formula executed by torch on bf16 tensors."""
+    h = cq.to(torch.float32)
+    var = h.pow(2).mean(-1, keepdim=True)
+    h = h * torch.rsqrt(var + eps)
+    return (gain * h.to(torch.bfloat16)).float()
+
+
+def test_q_latent_is_linear_then_rmsnorm():
+    """Inputs on a coarse grid (integers times powers of two), so that every
+    sum of the projection is exact in fp32: torch's fp32 matmul then gives the
+    exact value, and its bf16 cast rounds it once, as the Linear's bf16 output
+    does.  The norm is then the page's formula run by torch."""
+    rng = np.random.default_rng(21)
+    n, d, rank = 48, 256, 96
+    hid = (rng.integers(-64, 65, (n, d)) * 2.0 ** -5).astype(np.float32)      # 7-bit values
+    wq = (rng.integers(-32, 33, (rank, d)) * 2.0 ** -8).astype(np.float32)    # 6-bit values
+    g = (rng.integers(64, 192, rank) * 2.0 ** -7).astype(np.float32)
+    c_or, q_or = orc.q_latent(d, rank, "bf16", bf16_bits(hid), bf16_bits(wq), bf16_bits(g))
+    c_t = (torch.from_numpy(hid) @ torch.from_numpy(wq).T).to(torch.bfloat16)
+    np.testing.assert_array_equal(c_or, c_t.float().numpy())
+    assert (c_t.float() != torch.from_numpy(hid) @ torch.from_numpy(wq).T).any()   # rounding happened
+    q_t = torch_rmsnorm_bf16(c_t, torch.from_numpy(g).to(torch.bfloat16), 1e-6).numpy()
+    same = q_or == q_t
+    assert same.mean() > 0.995                   # sum order of the mean of squares may flip an ulp
+    ulp = np.abs(q_or - q_t) / np.maximum(np.abs(q_t), 1e-30)
+    assert ulp[~same].max(initial=0) <= 2 ** -7 + 1e-9
+
+
+def test_q_latent_identity_projection_is_the_norm_of_the_leading_features():
+    """W = [I | 0] ([rank, d], nn.Linear orientation): c is the first rank
+    features of the row, and q their RMSNorm (step A, pinned above)."""
+    rng = np.random.default_rng(22)
+    n, d, rank = 20, 128, 48
+    hid = bf16_bits(rng.standard_normal((n, d)))
+    wq = np.zeros((rank, d), np.float32)
+    wq[np.arange(rank), np.arange(rank)] = 1.0
+    g = bf16_bits(rng.uniform(0.5, 1.5, rank))
+    c_or, q_or = orc.q_latent(d, rank, "bf16", hid, bf16_bits(wq), g)
+    lead = np.ascontiguousarray(hid[:, :rank])
+    np.testing.assert_array_equal(c_or, as_f64(lead, "bf16").astype(np.float32))
+    np.testing.assert_array_equal(q_or, orc.rmsnorm(orc.cfg(rank, 1, 1, 0, 1, "bf16"), lead, g))
+
+
+def test_q_latent_fp32_and_selected_rows():
+    rng = np.random.default_rng(23)
+    n, d, rank = 16, 64, 32
+    hid = rng.standard_normal((n, d)).astype(np.float32)
+    wq = (rng.standard_normal((rank, d)) * 0.1).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, rank).astype(np.float32)
+    c_or, q_or = orc.q_latent(d, rank, "fp32", hid, wq, g, eps=1e-6)
+    np.testing.assert_allclose(c_or, hid.astype(np.float64) @ wq.astype(np.float64).T, rtol=1e-6, atol=1e-7)
+    cd = c_or.astype(np.float64)
+    np.testing.assert_allclose(q_or, g * cd / np.sqrt((cd ** 2).mean(1, keepdims=True) + 1e-6), rtol=2e-6)
+    rows = np.array([7, 2, 11])
+    c2, q2 = orc.q_latent(d, rank, "fp32", hid, wq, g, rows=rows)
+    np.testing.assert_array_equal(q2, q_or[rows])
+    np.testing.assert_array_equal(c2, c_or[rows])
