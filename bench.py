@@ -2,7 +2,8 @@
 """Throughput of the GLM MoE feed-forward sublayer forward pass on B300.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload glm5_prefill] [--no-decode] [--no-dense] [--no-pack] [--only-dense]
+                  [--workload glm5_prefill] [--no-decode] [--no-dense] [--no-pack] [--no-qlatent]
+                  [--only-dense]
                   [--no-cpu-baseline]
 
 One step is one forward pass of the whole sublayer (RMSNorm, sigmoid router
@@ -16,8 +17,10 @@ scaling is weak and the value is the tokens of all ranks per second.
 
 On the GLM-5 prefill workload the line also carries the GLM-5-shaped decode
 step (``decode``), the dense feed-forward block of the first decoder
-layers (``dense``: moe_dense_forward at T = 8192 and T = 64) and the
-packing of the experts' HF weights into the grouped layout (``pack``).
+layers (``dense``: moe_dense_forward at T = 8192 and T = 64), the query
+compression of the sparse latent attention (``q_latent``: moe_q_latent at
+T = 8192 and T = 64) and the packing of the experts' HF weights into the
+grouped layout (``pack``).
 
 Rank 0 prints one JSON line.  ``--impl reference`` times the CPU oracle (the
 plain definition of the sublayer, run on the host cores) on a bounded sample
@@ -45,13 +48,33 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 METRIC = "MoE sublayer tokens/s"
 SWEEP_T = (1, 8, 16, 32, 128)   # decode token range (GLM-5 decode weights and bias)
 
-# DRAM bytes (read + write) per launch of the grouped GEMMs from the ncu
-# capture summarised in profiles/tc_gemm_pair_glm5_slice.md: the GLM-5 slice
-# (32 experts, 1024 tokens) scaled by 8 to the full GLM-5 prefill launch
-# (routed experts and tokens grow 8x; the shared expert's 50 MB of weights do
-# not, so the figure overstates by at most 0.35 GB).  Null once the kernel
-# changes after that capture.
-TRAFFIC_PER_LAUNCH = {"glm5_prefill": {"gate_up_swiglu": 15.51e9, "down_weighted": 7.79e9}}
+# DRAM bytes (read + write) per launch of the grouped GEMMs from an ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum), per workload and
+# stage, with the hash of the GEMM kernel sources it was taken on.  The bench
+# reports the figure only while the sources still hash to that value: any
+# change to the kernels makes it null until it is captured again.
+TRAFFIC_PER_LAUNCH = {}
+TRAFFIC_SOURCES = ("k_gemm_pair.cuh", "k_gemm_tc.cuh", "ptx.cuh")
+
+
+def gemm_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "mixture_experts_transformer_sigmoid_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, stage: str):
+    """DRAM bytes per launch from an ncu capture taken on the current kernel
+    sources, else None."""
+    rec = TRAFFIC_PER_LAUNCH.get(workload, {}).get(stage)
+    if rec is None or rec["source_hash"] != gemm_source_hash():
+        return None
+    return rec["bytes"]
+
+
 GEMM_KERNEL = "tc_gemm_pair_kernel"
 
 
@@ -64,10 +87,12 @@ def load_peaks():
 
 # ------------------------------------------------------------ arithmetic
 def gate_up_flops(w, T):
+    """The gate|up launch: routed experts and the shared expert (stage gate_up_swiglu)."""
     return 4.0 * T * w.k * w.d * w.I + 4.0 * T * w.d * w.Is
 
 
 def down_flops(w, T):
+    """The down launch: routed experts and the shared expert (stage down_weighted)."""
     return 2.0 * T * w.k * w.I * w.d + 2.0 * T * w.Is * w.d
 
 
@@ -291,7 +316,8 @@ def run_ours(args, world, rank, local):
                 "frac_of_sustained": round(dom_tf / peaks["bf16_tflops_sustained"], 4),
                 "peak_source": f"{peak_src} bf16 dense (burst)",
                 "flops_per_launch": dom_flops, "avg_launch_ms": round(dom_ms, 4),
-                "traffic": TRAFFIC_PER_LAUNCH.get(w.name, {}).get(dominant)}
+                "traffic": measured_traffic(w.name, dominant),
+                "kernel_source_hash": gemm_source_hash()}
     whole_tf = total_flops(w, T) / (ms / 1e3) / 1e12
     l2 = (f"inputs larger than L2 ({weight_bytes(w) / 1e9:.1f} GB of weights read every step)"
           if weight_bytes(w) > 126e6 else "inputs smaller than L2")
@@ -319,6 +345,10 @@ def run_ours(args, world, rank, local):
     # ---- the dense feed-forward block of the first decoder layers (moe_dense_forward)
     if args.dense and w.name == "glm5_prefill":
         res["dense"] = run_dense(args, local, peaks, peak_src, world)
+
+    # ---- the MLA query compression on the GLM-5 shapes (moe_q_latent)
+    if args.qlatent and w.name == "glm5_prefill":
+        res["q_latent"] = run_qlatent(args, local, peaks, peak_src, world)
 
     # ---- HF -> grouped layout packing of the GLM-5 expert weights (moe_pack_experts)
     if args.pack and w.name == "glm5_prefill":
@@ -531,6 +561,57 @@ def run_dense(args, local, peaks, peak_src, world):
     return res
 
 
+def run_qlatent(args, local, peaks, peak_src, world):
+    """moe_q_latent (the query compression of the sparse latent attention) on
+    the GLM-5 shapes (d 6144, q_lora_rank 2048): prefill (T = 8192, against the
+    bf16 peak) and decode (T = 64, L2 flushed, against HBM)."""
+    from mixture_experts_transformer_sigmoid_b300 import binding as B
+    wp, wd = wl.QLATENT_WORKLOADS["glm5_q_prefill"], wl.QLATENT_WORKLOADS["glm5_q_decode"]
+    inp = wl.make_q_inputs(wp, device="cuda")
+    dinp = wl.make_q_inputs(wd, device="cuda", weights_from=inp)
+    layer = B.MoeSublayer(max_tokens=wp.T, hidden=wp.d, n_experts=0, inter=0, shared_inter=0,
+                          max_top_k=0, dtype=wp.dtype, eps=wp.eps, device=local, dense_inter=64)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    res = {}
+    for w, x in ((wp, inp["hidden"]), (wd, dinp["hidden"])):
+        c = torch.empty((w.T, w.rank), dtype=x.dtype, device="cuda")
+        q = torch.empty_like(c)
+        for _ in range(args.warmup):
+            layer.q_latent(x, inp["w_qa"], inp["q_norm_w"], c_out=c, q_out=q)
+        assert layer.sync_status() == B.MOE_OK
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            layer.q_latent(x, inp["w_qa"], inp["q_norm_w"], c_out=c, q_out=q)
+        torch.cuda.synchronize()
+        n_iter = max(50, args.steps * 4)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_iter)]
+        for a, b in evs:
+            flush.zero_()                  # the weights (25 MB) would otherwise stay in L2
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.median([a.elapsed_time(b) for a, b in evs])
+        assert layer.sync_status() == B.MOE_OK
+        del graph
+        flops = 2.0 * w.T * w.d * w.rank
+        nbytes = 2 * (w.rank * w.d + w.T * w.d + 2 * w.T * w.rank + w.rank)
+        line = {"workload": w.name, "tokens": w.T, "ms_median": round(ms, 4),
+                "tokens_per_s": round(world * w.T / (ms / 1e3), 1), "flops": flops, "bytes": nbytes,
+                "tflops": round(flops / (ms / 1e3) / 1e12, 1),
+                "tensor_frac": round(flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+                "hbm_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+                "hbm_frac": round(nbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                "peak_source": f"{peak_src} (bf16 burst, HBM copy)",
+                "l2": "256 MB buffer written between steps (outside the timed events)",
+                "launch": "CUDA graph replay of one moe_q_latent"}
+        res["prefill" if w.T >= 1024 else "decode"] = line
+    layer.close()
+    return res
+
+
 def run_pack(args, inp, peaks, peak_src):
     """moe_pack_experts on the GLM-5 expert weights: the HF per-expert stacks
     (made from the workload's grouped weights by torch transposes, outside
@@ -613,6 +694,7 @@ def main():
     ap.add_argument("--no-decode", dest="decode", action="store_false")
     ap.add_argument("--no-dense", dest="dense", action="store_false")
     ap.add_argument("--no-pack", dest="pack", action="store_false")
+    ap.add_argument("--no-qlatent", dest="qlatent", action="store_false")
     ap.add_argument("--only-dense", action="store_true",
                     help="time only the dense feed-forward block (about 1 GB on the device; "
                          "the case for profiling its kernels)")

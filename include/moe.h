@@ -58,7 +58,9 @@ typedef enum {
     MOE_ERR_UNSUPPORTED = 2,  /* valid, but a shape this build does not handle */
     MOE_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
     MOE_ERR_OOM = 4,          /* workspace allocation failed in moe_init */
-    MOE_ERR_TIMEOUT = 5       /* a kernel's bounded wait expired (device error flag) */
+    MOE_ERR_TIMEOUT = 5,      /* a kernel's bounded wait expired (device error flag) */
+    MOE_ERR_RANGE = 6         /* a weighted expert row exceeded the fp16 range (|v| > 65504) of the
+                                 intermediate that carries it to the combine (device error flag) */
 } moe_status;
 
 typedef enum { MOE_DTYPE_FP32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
@@ -162,6 +164,29 @@ MOE_API moe_status moe_dense_forward(moe_handle* h, int32_t T, const void* x, co
                              const void* gate_w, const void* up_w, const void* down_w,
                              int32_t inter, void* out, void* stream);
 
+/* The query compression of GLM-5's sparse latent attention (GLM-5 "Query
+ * latent" page on OpenModelAtlas: the MLA __init__ builds q_a_proj =
+ * nn.Linear(hidden_size, q_lora_rank, bias=attention_bias) with
+ * attention_bias false, and q_a_layernorm = GlmMoeDsaRMSNorm(q_lora_rank);
+ * its forward computes q_resid = q_a_layernorm(q_a_proj(hidden_states))):
+ *   c_out = hidden @ w_qa^T      the query latent, rounded once to the handle dtype
+ *   q_out = RMSNorm(c_out)       with gain q_norm_w and the handle's eps (the
+ *                                page's latent norms take the 1e-6 default)
+ * Device pointers, row-major, 16-byte aligned, owned by the caller:
+ *   hidden [T, d] (d = cfg.hidden: the attention input, already normalised),
+ *   w_qa [q_rank, d] (nn.Linear [out, in]), q_norm_w [q_rank],
+ *   c_out [T, q_rank], q_out [T, q_rank]; the outputs must not overlap the
+ *   inputs or each other (MOE_ERR_INVALID_ARG).
+ * q_rank >= 1 (a multiple of 64 on the tensor-core path, else
+ * MOE_ERR_UNSUPPORTED); any T >= 0 (T == 0 queues nothing).  Any handle
+ * whose hidden size is d serves; small batches (T <= 128, T <= max_tokens
+ * and q_rank <= d) use its split-K buffer.  Asynchronous on `stream`, no
+ * allocation, no host synchronisation; a device-side timeout is reported by
+ * moe_sync_status. */
+MOE_API moe_status moe_q_latent(moe_handle* h, int32_t T, int32_t q_rank, const void* hidden,
+                        const void* w_qa, const void* q_norm_w, void* c_out, void* q_out,
+                        void* stream);
+
 /* Routing of the last forward on this handle, copied (device to device, on
  * `stream`) into caller buffers; any pointer may be NULL:
  *   idx [T, top_k] int32 expert ids in slot order, w [T, top_k] fp32 weights,
@@ -177,7 +202,8 @@ typedef enum {
     MOE_T_POS = 3,      /* [T, top_k] int32 permuted row of each (token, slot) */
     MOE_T_ROW_TOK = 4,  /* [T * top_k] int32 token of each permuted row */
     MOE_T_H = 5,        /* [T * top_k, I] routed SwiGLU activations, handle dtype */
-    MOE_T_SHARED = 6    /* [T, d] shared expert output, handle dtype */
+    MOE_T_YP = 6        /* [T * top_k, d] weighted expert rows w * expert(xn), permuted
+                           order: fp16 on the tensor-core path, else the handle dtype */
 } moe_tensor;
 
 /* Copies intermediate `which` of the last forward into dst (device memory
@@ -188,7 +214,9 @@ MOE_API moe_status moe_get_intermediate(moe_handle* h, moe_tensor which, void* d
 
 /* Synchronises `stream`, then reads and clears the handle's device error
  * flag: MOE_ERR_TIMEOUT if a kernel gave up a bounded wait since the last
- * call, MOE_ERR_CUDA on an asynchronous CUDA error, else MOE_OK. */
+ * call, MOE_ERR_RANGE if a weighted expert row overflowed its fp16
+ * intermediate (that forward's output holds infinities), MOE_ERR_CUDA on an
+ * asynchronous CUDA error, else MOE_OK. */
 MOE_API moe_status moe_sync_status(moe_handle* h, void* stream);
 
 /* Self-test of failure detection (no counterpart in the paper): queues on
@@ -254,8 +282,9 @@ MOE_API moe_status moe_destroy(moe_handle* h);
  * race, so serialise them.  The first call on each device looks up the
  * array's device address (cudaGetSymbolAddress); make that first call
  * before any stream capture.  1 <= E <= 1024, 1 <= top_k <= min(E, 32),
- * T >= 0 (T == 0 queues nothing); MOE_ERR_INVALID_ARG for other values or
- * null/misaligned pointers.  Asynchronous on `stream`. */
+ * T >= 0 (T == 0 queues nothing); MOE_ERR_INVALID_ARG for other values,
+ * null/misaligned pointers, or an output that overlaps an input or another
+ * output.  Asynchronous on `stream`. */
 MOE_API moe_status moe_route_static(int32_t T, int32_t E, int32_t top_k, float routed_scale,
                             const float* logits, const float* corr_bias, int32_t* idx, float* w,
                             int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* row_tok,

@@ -16,16 +16,19 @@ import torch
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmoe_b300.so")
 
-MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_OOM, MOE_ERR_TIMEOUT = range(6)
+(MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_OOM, MOE_ERR_TIMEOUT,
+ MOE_ERR_RANGE) = range(7)
 DTYPE_FP32, DTYPE_BF16 = 0, 1
-T_XN, T_LOGITS, T_OFFSETS, T_POS, T_ROW_TOK, T_H, T_SHARED = range(7)
+T_XN, T_LOGITS, T_OFFSETS, T_POS, T_ROW_TOK, T_H, T_YP = range(7)
 
 # Functions the header declares (kept in sync by the ABI test).
 EXPORTS = ("moe_init", "moe_forward", "moe_forward_host", "moe_forward_host_async",
-           "moe_forward_host_wait", "moe_dense_forward", "moe_get_routing",
+           "moe_forward_host_wait", "moe_dense_forward", "moe_q_latent", "moe_get_routing",
            "moe_get_intermediate", "moe_sync_status", "moe_selftest_wait_timeout",
            "moe_set_profiling", "moe_read_stats",
            "moe_destroy", "moe_route_static", "moe_pack_experts", "moe_status_string")
+# Stages of one forward (the gate_up and down launches carry the routed
+# experts and the shared expert).
 STAGES = ("rmsnorm", "router", "topk", "scan", "scatter", "gather", "gate_up_swiglu",
           "down_weighted", "combine")
 
@@ -70,6 +73,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_forward_host_async.argtypes = fwd
     lib.moe_forward_host_wait.argtypes = [P]
     lib.moe_dense_forward.argtypes = [P, I32, P, P, P, P, P, I32, P, P]
+    lib.moe_q_latent.argtypes = [P, I32, I32, P, P, P, P, P, P]
     lib.moe_get_routing.argtypes = [P, P, P, P, P]
     lib.moe_get_intermediate.argtypes = [P, ctypes.c_int, P, ctypes.c_size_t, P]
     lib.moe_sync_status.argtypes = [P, P]
@@ -111,6 +115,7 @@ class MoeSublayer:
                              DTYPE_BF16 if dtype == "bf16" else DTYPE_FP32, eps, device, gemm_path,
                              dense_inter)
         self.dtype = torch.bfloat16 if dtype == "bf16" else torch.float32
+        self.tensor_cores = dtype == "bf16" and gemm_path == 0   # the library's tcgen05 path
         self.device = torch.device("cuda", device)
         h = ctypes.c_void_p()
         _check(self.lib.moe_init(ctypes.byref(self.cfg), ctypes.byref(h)), "moe_init")
@@ -162,6 +167,19 @@ class MoeSublayer:
             "moe_dense_forward")
         return out
 
+    def q_latent(self, hidden, w_qa, q_norm_w, c_out=None, q_out=None, stream=None):
+        """moe_q_latent: the query compression of the sparse latent attention,
+        (c, q) = (q_a_proj(hidden), q_a_layernorm(c)); hidden [T, d], w_qa
+        [q_rank, d], q_norm_w [q_rank] (device tensors)."""
+        T, rank = hidden.shape[0], w_qa.shape[0]
+        if c_out is None:
+            c_out = torch.empty((T, rank), dtype=hidden.dtype, device=hidden.device)
+        if q_out is None:
+            q_out = torch.empty((T, rank), dtype=hidden.dtype, device=hidden.device)
+        _check(self.lib.moe_q_latent(self.handle, T, rank, _ptr(hidden), _ptr(w_qa), _ptr(q_norm_w),
+                                     _ptr(c_out), _ptr(q_out), self._stream(stream)), "moe_q_latent")
+        return c_out, q_out
+
     def forward_host(self, x_host, w: dict, top_k: int, routed_scale: float, out_host,
                      stream=None):
         """x_host / out_host: CPU tensors (pinned for asynchronous copies)."""
@@ -204,7 +222,7 @@ class MoeSublayer:
         shapes = {T_XN: ((T, c.hidden), self.dtype), T_LOGITS: ((T, c.n_experts), torch.float32),
                   T_OFFSETS: ((c.n_experts + 1,), torch.int32), T_POS: ((T, k), torch.int32),
                   T_ROW_TOK: ((T * k,), torch.int32), T_H: ((T * k, c.inter), self.dtype),
-                  T_SHARED: ((T, c.hidden), self.dtype)}
+                  T_YP: ((T * k, c.hidden), torch.float16 if self.tensor_cores else self.dtype)}
         shape, dt = shapes[which]
         dst = torch.empty(shape, dtype=dt, device=self.device)
         _check(self.lib.moe_get_intermediate(self.handle, which, _ptr(dst),
@@ -245,8 +263,15 @@ def route_static(logits: torch.Tensor, corr_bias: torch.Tensor, top_k: int,
     caller's output tensors (idx, w, counts, offsets, pos, row_tok, row_w);
     missing ones are created here with torch.  Calls that overlap on the GPU
     share one static scratch array and race."""
+    if logits.dim() != 2 or logits.dtype != torch.float32 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous fp32 [T, E] tensor")
     T, E = logits.shape
     dev = logits.device
+    if dev.type != "cuda":
+        raise ValueError("logits must be on a CUDA device")
+    if (corr_bias.dtype != torch.float32 or not corr_bias.is_contiguous()
+            or corr_bias.numel() != E or corr_bias.device != dev):
+        raise ValueError("corr_bias must be a contiguous fp32 [E] tensor on the logits' device")
     shapes = {"idx": ((T, top_k), torch.int32), "w": ((T, top_k), torch.float32),
               "counts": ((E,), torch.int32), "offsets": ((E + 1,), torch.int32),
               "pos": ((T, top_k), torch.int32), "row_tok": ((T * top_k,), torch.int32),
@@ -255,12 +280,19 @@ def route_static(logits: torch.Tensor, corr_bias: torch.Tensor, top_k: int,
     for name, (shape, dt) in shapes.items():
         if name not in res:
             res[name] = torch.empty(shape, dtype=dt, device=dev)
+        else:
+            t = res[name]
+            if (t.dtype != dt or not t.is_contiguous() or t.numel() != int(torch.Size(shape).numel())
+                    or t.device != dev):
+                raise ValueError(f"out[{name!r}] must be a contiguous {dt} tensor of {shape} "
+                                 f"elements on {dev}")
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    st = load_library().moe_route_static(
-        T, E, top_k, routed_scale, _ptr(logits), _ptr(corr_bias), _ptr(res["idx"]),
-        _ptr(res["w"]), _ptr(res["counts"]), _ptr(res["offsets"]), _ptr(res["pos"]),
-        _ptr(res["row_tok"]), _ptr(res["row_w"]), ctypes.c_void_p(stream.cuda_stream))
+    with torch.cuda.device(dev):   # the library takes its scratch address from the current device
+        st = load_library().moe_route_static(
+            T, E, top_k, routed_scale, _ptr(logits), _ptr(corr_bias), _ptr(res["idx"]),
+            _ptr(res["w"]), _ptr(res["counts"]), _ptr(res["offsets"]), _ptr(res["pos"]),
+            _ptr(res["row_tok"]), _ptr(res["row_w"]), ctypes.c_void_p(stream.cuda_stream))
     if st == MOE_ERR_UNSUPPORTED:
         raise MoeError(st, f"moe_route_static: ceil(T/128)*E = {-(-T // 128) * E} exceeds the "
                            f"static scratch limit of {ROUTE_STATIC_MAX_CELLS} cells")

@@ -23,6 +23,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "k_gemm_tc.cuh"
@@ -65,6 +66,7 @@ struct PairCursor {
     int f0;      // first feature of this CTA's A rows
     int r0;      // first token row of this CTA's B half
     int nb;      // B bytes this CTA loads per k-block, in 8 KB units (one 64- or 128-row box)
+    int half;    // B rows of this CTA's half of the tile (MMA N / 2)
     bool valid;
     TileInfo ti;
 
@@ -72,7 +74,7 @@ struct PairCursor {
         valid = decode_tile(p, prefix, L, PR_BN, ti);
         if (!valid) return;
         const TcSeg& sg = p.seg[ti.seg];
-        const int half = ((ti.rows + 15) & ~15) >> 1;  // MMA N / 2
+        half = ((ti.rows + 15) & ~15) >> 1;  // MMA N / 2, a multiple of 8
         nb = half > 64 ? 2 : 1;
         f0 = ti.ftile * sg.a_fstride + static_cast<int>(rank) * sg.a_rank_off;
         r0 = ti.row0 + static_cast<int>(rank) * half;
@@ -89,6 +91,18 @@ struct PairCursor {
         set_tile(p, prefix, rank);
     }
 };
+
+// a8 (+)= the eight bf16 values of v, widened to fp32 (set: a8 = v).
+__device__ __forceinline__ void add_bf16x8(const uint4 v, float (&a8)[8], bool set) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+        a8[2 * j] = set ? f.x : a8[2 * j] + f.x;
+        a8[2 * j + 1] = set ? f.y : a8[2 * j + 1] + f.y;
+    }
+}
+
 
 // Launched with a cluster dimension of 2 (cudaLaunchKernelEx).
 template <int EPI>
@@ -351,9 +365,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_pair_kernel(const __gri
                     named_bar_sync(2, 128);
                 } else {
                     // stage this warp's 32 features x 32 tokens, then write 8 features of
-                    // one token per 16-byte store: scaled by that token's routing weight
-                    // (EPI_WEIGHTED) or added to 8 residual values read with one
-                    // 16-byte load (EPI_RESIDUAL)
+                    // one token per 16-byte store (two for fp32 output): scaled by that
+                    // token's routing weight (EPI_WEIGHTED) or added to 8 residual values
+                    // read with one 16-byte load (EPI_RESIDUAL)
                     static_assert(EPI == EPI_WEIGHTED || EPI == EPI_RESIDUAL, "epilogue");
                     float* stg = xbuf + q * (32 * 33);
 #pragma unroll
@@ -369,21 +383,42 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_pair_kernel(const __gri
                             uint32_t pk[4];
                             if constexpr (EPI == EPI_WEIGHTED) {
                                 const float wv = sg.row_w ? sg.row_w[row] : 1.0f;
+                                if (sg.out_kind == OUT_F32) {
+                                    float* o32 = static_cast<float*>(sg.out) + static_cast<size_t>(row) * sg.ld_out + col;
+                                    const float* sp = stg + t * 33 + sub * 8;
+                                    *reinterpret_cast<float4*>(o32) = make_float4(sp[0] * wv, sp[1] * wv, sp[2] * wv, sp[3] * wv);
+                                    *reinterpret_cast<float4*>(o32 + 4) = make_float4(sp[4] * wv, sp[5] * wv, sp[6] * wv, sp[7] * wv);
+                                    continue;
+                                }
+                                if (sg.out_kind == OUT_F16) {
+                                    float amax = 0.f;
 #pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    const __nv_bfloat162 hb = __floats2bfloat162_rn(
-                                        stg[t * 33 + sub * 8 + 2 * j] * wv, stg[t * 33 + sub * 8 + 2 * j + 1] * wv);
-                                    pk[j] = *reinterpret_cast<const uint32_t*>(&hb);
+                                    for (int j = 0; j < 4; ++j) {
+                                        const float y0 = stg[t * 33 + sub * 8 + 2 * j] * wv;
+                                        const float y1 = stg[t * 33 + sub * 8 + 2 * j + 1] * wv;
+                                        amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+                                        const __half2 hh = __floats2half2_rn(y0, y1);
+                                        pk[j] = *reinterpret_cast<const uint32_t*>(&hh);
+                                    }
+                                    if (!(amax <= 65504.0f)) atomicOr(p.err, DEVERR_RANGE);
+                                } else {
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) {
+                                        const __nv_bfloat162 hb = __floats2bfloat162_rn(
+                                            stg[t * 33 + sub * 8 + 2 * j] * wv, stg[t * 33 + sub * 8 + 2 * j + 1] * wv);
+                                        pk[j] = *reinterpret_cast<const uint32_t*>(&hb);
+                                    }
                                 }
                             } else {
                                 const uint4 r4 = *reinterpret_cast<const uint4*>(
                                     static_cast<const __nv_bfloat16*>(sg.res) + static_cast<size_t>(row) * sg.ld_out + col);
-                                const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
+                                float a8[8];
+                                add_bf16x8(r4, a8, true);
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) a8[j] += stg[t * 33 + sub * 8 + j];
 #pragma unroll
                                 for (int j = 0; j < 4; ++j) {
-                                    const float2 rf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rw[j]));
-                                    const __nv_bfloat162 hb = __floats2bfloat162_rn(rf.x + stg[t * 33 + sub * 8 + 2 * j],
-                                                                                    rf.y + stg[t * 33 + sub * 8 + 2 * j + 1]);
+                                    const __nv_bfloat162 hb = __floats2bfloat162_rn(a8[2 * j], a8[2 * j + 1]);
                                     pk[j] = *reinterpret_cast<const uint32_t*>(&hb);
                                 }
                             }

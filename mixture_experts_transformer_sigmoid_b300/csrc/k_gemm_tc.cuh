@@ -30,6 +30,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -45,13 +46,16 @@ constexpr int TC_THREADS = 192;
 constexpr uint64_t TC_TIMEOUT_NS = 2000000000ull;   // 2 s
 constexpr uint64_t TC_DRAIN_NS = 100000000ull;      // 100 ms
 constexpr int DEVERR_TIMEOUT = 1;
+constexpr int DEVERR_RANGE = 2;     // an fp16 output overflowed (|v| > 65504)
 
 // SWIGLU: out = silu(gate) * up, from the gate and up halves of the A rows.
-// WEIGHTED: out = row_w[row] * acc (row_w null: acc).
+// WEIGHTED: out = row_w[row] * acc (row_w null: acc), stored as the
+//   segment's out_kind says: bf16, fp16 (an overflow sets DEVERR_RANGE) or fp32.
 // RESIDUAL: out = res[row, col] + acc, added in fp32 and rounded once.
 // PARTIAL: fp32 acc of one k-range of a split dense segment, to
 //   out[k-range][row][col] (single-CTA kernel; the ranges are added later).
 enum EpiKind { EPI_SWIGLU = 1, EPI_WEIGHTED = 2, EPI_RESIDUAL = 3, EPI_PARTIAL = 4 };
+enum OutKind { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2 };
 
 struct TcSeg {
     int grouped;          // 1: expert groups from offsets[]; 0: one group of n_rows rows
@@ -69,6 +73,9 @@ struct TcSeg {
     const void* res;      // residual epilogue: bf16 [rows, ld_out], indexed like out
     int f_group;          // dense segment: feature tiles per tile group (0: all of them)
     int k_split;          // dense segment, single-CTA kernel: k-ranges per tile (0 or 1: none)
+    int out_kind;         // weighted epilogue: OutKind of `out`
+    const int* b_rows;    // CTA-pair kernel: B row r of the tile is row b_rows[r] of map b (box one
+                          // row high, four rows per tile::gather4 copy); null: B rows are contiguous
 };
 
 struct TcParams {
@@ -389,17 +396,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     named_bar_sync(2, 128);
                 } else if constexpr (EPI == EPI_WEIGHTED) {
                     const int col = ti.ftile * sg.a_fstride + q * 32 + lane;
-                    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
                     if (col < sg.F) {
                         const int cmax = min(32, ti.rows - c0);
+                        float amax = 0.f;
 #pragma unroll
                         for (int c = 0; c < 32; ++c) {
                             if (c >= cmax) break;
                             const int row = ti.row0 + c0 + c;
                             const float wv = sg.row_w ? sg.row_w[row] : 1.0f;
-                            out[static_cast<size_t>(row) * sg.ld_out + col] =
-                                __float2bfloat16_rn(__uint_as_float(v[c]) * wv);
+                            const float y = __uint_as_float(v[c]) * wv;
+                            const size_t at = static_cast<size_t>(row) * sg.ld_out + col;
+                            if (sg.out_kind == OUT_F16) {
+                                static_cast<__half*>(sg.out)[at] = __float2half_rn(y);
+                                amax = fmaxf(amax, fabsf(y));
+                            } else if (sg.out_kind == OUT_F32) {
+                                static_cast<float*>(sg.out)[at] = y;
+                            } else {
+                                static_cast<__nv_bfloat16*>(sg.out)[at] = __float2bfloat16_rn(y);
+                            }
                         }
+                        if (!(amax <= 65504.0f)) atomicOr(p.err, DEVERR_RANGE);
                     }
                 } else if constexpr (EPI == EPI_PARTIAL) {
                     const int col = ti.ftile * sg.a_fstride + q * 32 + lane;
@@ -422,7 +438,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
 #pragma unroll
                         for (int c = 0; c < 32; ++c) {
                             if (c >= cmax) break;
-                            const size_t at = static_cast<size_t>(ti.row0 + c0 + c) * sg.ld_out + col;
+                            const int row = ti.row0 + c0 + c;
+                            const size_t at = static_cast<size_t>(row) * sg.ld_out + col;
                             out[at] = __float2bfloat16_rn(__bfloat162float(res[at]) + __uint_as_float(v[c]));
                         }
                     }

@@ -4,6 +4,7 @@
 // and the FFMA expert kernels used for fp32 storage.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "numeric.cuh"
@@ -26,6 +27,11 @@ template <> struct Elem<__nv_bfloat16> {
     __device__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
     __device__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
     __device__ static float round_io(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+};
+template <> struct Elem<__half> {   // the weighted expert rows of the tensor-core path
+    static constexpr int V = 8;
+    __device__ static float to_f(__half v) { return __half2float(v); }
+    __device__ static __half from_f(float v) { return __float2half_rn(v); }
 };
 
 template <typename T>
@@ -171,41 +177,46 @@ __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ ga
     }
 }
 
-// The same RMSNorm with one warp per token (no block barriers): each lane
-// keeps up to RMS_WARP_VECS 16-byte vectors of the row in registers, and the
-// compensated sum of squares is reduced with shuffles.  For d / V <=
-// 32 * RMS_WARP_VECS (d <= 6144 in bf16); rmsnorm_kernel covers longer rows.
-constexpr int RMS_WARP_VECS = 24;
+// The same RMSNorm with one warp per token (no block barriers).  The first
+// pass streams the row in batches of RMS_WARP_U 16-byte vectors per lane and
+// accumulates the compensated sum of squares (each lane takes vectors lane,
+// lane + 32, ... in order, then a shuffle reduction); the second pass reads
+// the row again (from L2: it was just read) and scales it.  Holding the row
+// in registers instead would take ~190 registers per thread for d = 6144 and
+// leave too few warps per SM to cover DRAM latency.
+constexpr int RMS_WARP_U = 8;
 
 template <typename T>
-__global__ void rmsnorm_warp_kernel(const T* __restrict__ x, const T* __restrict__ gain,
-                                    T* __restrict__ xn, int n_tok, int d, float eps) {
+__global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const T* __restrict__ x, const T* __restrict__ gain,
+                                                           T* __restrict__ xn, int n_tok, int d, float eps) {
     constexpr int V = Elem<T>::V;
     const int lane = threadIdx.x & 31;
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= n_tok) return;
     const int nvec = d / V;
-    const T* xr = x + static_cast<size_t>(t) * d;
-    int4 raw[RMS_WARP_VECS];
-#pragma unroll
-    for (int j = 0; j < RMS_WARP_VECS; ++j) {
-        const int v = lane + 32 * j;
-        if (v < nvec) raw[j] = __ldg(reinterpret_cast<const int4*>(xr) + v);
-    }
+    const int4* xr = reinterpret_cast<const int4*>(x + static_cast<size_t>(t) * d);
     float hi = 0.f, lo = 0.f;
+    for (int v0 = 0; v0 < nvec; v0 += 32 * RMS_WARP_U) {
+        int4 raw[RMS_WARP_U];
 #pragma unroll
-    for (int j = 0; j < RMS_WARP_VECS; ++j) {
-        if (lane + 32 * j >= nvec) continue;
-        const T* e = reinterpret_cast<const T*>(&raw[j]);
+        for (int j = 0; j < RMS_WARP_U; ++j) {
+            const int v = v0 + lane + 32 * j;
+            if (v < nvec) raw[j] = __ldg(xr + v);
+        }
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-            const float f = Elem<T>::to_f(e[i]);
-            const float p = __fmul_rn(f, f);
-            const float pe = fmaf(f, f, -p);
-            float s, er;
-            two_sum_f(hi, p, s, er);
-            hi = s;
-            lo = __fadd_rn(lo, __fadd_rn(er, pe));
+        for (int j = 0; j < RMS_WARP_U; ++j) {
+            if (v0 + lane + 32 * j >= nvec) continue;
+            const T* e = reinterpret_cast<const T*>(&raw[j]);
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const float f = Elem<T>::to_f(e[i]);
+                const float p = __fmul_rn(f, f);
+                const float pe = fmaf(f, f, -p);
+                float s, er;
+                two_sum_f(hi, p, s, er);
+                hi = s;
+                lo = __fadd_rn(lo, __fadd_rn(er, pe));
+            }
         }
     }
 #pragma unroll
@@ -220,17 +231,25 @@ __global__ void rmsnorm_warp_kernel(const T* __restrict__ x, const T* __restrict
     const float ms = static_cast<float>((static_cast<double>(hi) + static_cast<double>(lo)) /
                                         static_cast<double>(d));
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+    for (int v0 = 0; v0 < nvec; v0 += 32 * RMS_WARP_U) {
+        int4 raw[RMS_WARP_U];
 #pragma unroll
-    for (int j = 0; j < RMS_WARP_VECS; ++j) {
-        const int v = lane + 32 * j;
-        if (v >= nvec) continue;
-        const T* e = reinterpret_cast<const T*>(&raw[j]);
-        float f[V], g[V];
-        load_vec<T>(gain + v * V, g);
+        for (int j = 0; j < RMS_WARP_U; ++j) {
+            const int v = v0 + lane + 32 * j;
+            if (v < nvec) raw[j] = __ldg(xr + v);
+        }
 #pragma unroll
-        for (int i = 0; i < V; ++i)
-            f[i] = __fmul_rn(g[i], Elem<T>::round_io(__fmul_rn(Elem<T>::to_f(e[i]), r)));
-        store_vec<T>(xn + static_cast<size_t>(t) * d + v * V, f);
+        for (int j = 0; j < RMS_WARP_U; ++j) {
+            const int v = v0 + lane + 32 * j;
+            if (v >= nvec) continue;
+            const T* e = reinterpret_cast<const T*>(&raw[j]);
+            float f[V], g[V];
+            load_vec<T>(gain + v * V, g);
+#pragma unroll
+            for (int i = 0; i < V; ++i)
+                f[i] = __fmul_rn(g[i], Elem<T>::round_io(__fmul_rn(Elem<T>::to_f(e[i]), r)));
+            store_vec<T>(xn + static_cast<size_t>(t) * d + v * V, f);
+        }
     }
 }
 
@@ -279,34 +298,55 @@ __global__ void rmsnorm_router_kernel(const T* __restrict__ x, const T* __restri
 }
 
 // ------------------------------------------------------------------ top-k
-// One warp per token.  The logit is the router's (hi, lo) pair rounded once
-// (also written to `logits` for inspection).  s = sigmoid(l), b = s + bias;
-// k rounds of a warp
+// Where the top-k kernel reads a token's logits from: the router's (hi, lo)
+// partial-sum pairs, rounded once here (and written to `logits` for
+// inspection), or plain fp32 logits given by the caller.
+struct LogitsFromPairs {
+    const float2* __restrict__ part;
+    float* __restrict__ logits;
+    __device__ float load(size_t i) const {
+        const float2 pv = part[i];
+        const float l = __fadd_rn(pv.x, pv.y);  // the (hi, lo) pair, rounded once
+        logits[i] = l;
+        return l;
+    }
+};
+struct LogitsPlain {
+    const float* __restrict__ logits;
+    __device__ float load(size_t i) const { return logits[i]; }
+};
+
+// One warp per token.  s = sigmoid(l), b = s + bias; k rounds of a warp
 // argmax on (b descending, expert index ascending); slot j's expert and
-// sigmoid end up in lane j.  w_j = routed_scale * s_j / sum_i s_i.  Each
-// block covers CHUNK_TOKENS tokens and writes that chunk's expert histogram.
-// EPL = experts per lane (ceil(E / 32)).
-template <int EPL>
-__global__ void topk_kernel(const float2* __restrict__ part, const float* __restrict__ bias,
-                            int T, int E, int k, float routed_scale, float* __restrict__ logits,
-                            int* __restrict__ idx_out, float* __restrict__ w_out,
-                            int* __restrict__ chunk_cnt) {
+// sigmoid end up in lane j.  w_j = routed_scale * s_j / sum_i s_i.  Blocks
+// cover CHUNK_TOKENS / split tokens of a histogram chunk (split blocks per
+// chunk, so that small batches still spread over the SMs); each counts its
+// tokens' experts in shared memory and adds the counts to its chunk's
+// histogram in global memory (zeroed before the launch when split > 1;
+// integer adds, so the result does not depend on their order).
+// EPL = experts per lane (ceil(E / 32)).  The selection does not depend on
+// where the logits came from: given the same fp32 logits, both sources take
+// the same decisions and give the same weights bit for bit.
+template <int EPL, typename Src>
+__global__ void topk_kernel(const Src src, const float* __restrict__ bias, int T, int E, int k,
+                            float routed_scale, int* __restrict__ idx_out, float* __restrict__ w_out,
+                            int* __restrict__ chunk_cnt, int split) {
     extern __shared__ int cnt[];  // [E]
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    const int chunk = blockIdx.x;
-    for (int tl = warp; tl < CHUNK_TOKENS; tl += nw) {
-        const int t = chunk * CHUNK_TOKENS + tl;
+    const int chunk = blockIdx.x / split;
+    const int sub_tokens = CHUNK_TOKENS / split;
+    const int first = chunk * CHUNK_TOKENS + (blockIdx.x - chunk * split) * sub_tokens;
+    for (int tl = warp; tl < sub_tokens; tl += nw) {
+        const int t = first + tl;
         if (t >= T) break;
         float bv[EPL], sv[EPL];
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
             if (e < E) {
-                const float2 pv = part[static_cast<size_t>(t) * E + e];
-                const float l = __fadd_rn(pv.x, pv.y);  // the (hi, lo) pair, rounded once
-                logits[static_cast<size_t>(t) * E + e] = l;
+                const float l = src.load(static_cast<size_t>(t) * E + e);
                 const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
                 const float b = __fadd_rn(s, bias[e]);
                 sv[i] = s;
@@ -357,83 +397,12 @@ __global__ void topk_kernel(const float2* __restrict__ part, const float* __rest
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        chunk_cnt[static_cast<size_t>(chunk) * E + e] = cnt[e];
-}
-
-// The same selection as topk_kernel, for callers that hold the router
-// logits as plain fp32 values [T, E] rather than the router's (hi, lo)
-// pairs.  Given the logits topk_kernel rounded, the two kernels take the
-// same decisions and produce the same weights bit for bit.
-template <int EPL>
-__global__ void topk_logits_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
-                                   int T, int E, int k, float routed_scale,
-                                   int* __restrict__ idx_out, float* __restrict__ w_out,
-                                   int* __restrict__ chunk_cnt) {
-    extern __shared__ int cnt[];  // [E]
-    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    const int chunk = blockIdx.x;
-    for (int tl = warp; tl < CHUNK_TOKENS; tl += nw) {
-        const int t = chunk * CHUNK_TOKENS + tl;
-        if (t >= T) break;
-        float bv[EPL], sv[EPL];
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E) {
-                const float l = logits[static_cast<size_t>(t) * E + e];
-                const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
-                const float b = __fadd_rn(s, bias[e]);
-                sv[i] = s;
-                bv[i] = (b == b) ? b : -INFINITY;
-            } else {
-                sv[i] = 0.f;
-                bv[i] = 0.f;
-            }
-        }
-        int my_e = 0;
-        float my_s = 0.f;
-        uint32_t removed = 0u;
-        for (int j = 0; j < k; ++j) {
-            float bb = 0.f, bs = 0.f;
-            int be = -1;
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && !((removed >> i) & 1u) && (be < 0 || bv[i] > bb)) {
-                    bb = bv[i];
-                    be = e;
-                    bs = sv[i];
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ob = __shfl_xor_sync(0xffffffffu, bb, off);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-                if (oe >= 0 && (be < 0 || ob > bb || (ob == bb && oe < be))) {
-                    bb = ob;
-                    be = oe;
-                    bs = os;
-                }
-            }
-            if ((be & 31) == lane) removed |= 1u << (be >> 5);
-            if (lane == j) { my_e = be; my_s = bs; }
-        }
-        float ssum = 0.f;
-        for (int j = 0; j < k; ++j) ssum = __fadd_rn(ssum, __shfl_sync(0xffffffffu, my_s, j));
-        if (lane < k) {
-            idx_out[static_cast<size_t>(t) * k + lane] = my_e;
-            w_out[static_cast<size_t>(t) * k + lane] =
-                __fdiv_rn(__fmul_rn(routed_scale, my_s), ssum);
-            atomicAdd(&cnt[my_e], 1);
-        }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        if (split == 1)
+            chunk_cnt[static_cast<size_t>(chunk) * E + e] = cnt[e];
+        else if (cnt[e] != 0)
+            atomicAdd(&chunk_cnt[static_cast<size_t>(chunk) * E + e], cnt[e]);
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        chunk_cnt[static_cast<size_t>(chunk) * E + e] = cnt[e];
 }
 
 // --------------------------------------------------- histogram scan (1 block)
@@ -577,10 +546,12 @@ __global__ void gather_rows_kernel(const T* __restrict__ xn, const int* __restri
 }
 
 // out[t] = x[t] + sh[t] + sum_j yp[pos[t, j]] in fp32, slots in order, one
-// rounding at the end (yp rows already carry their routing weight).
-template <typename T>
-__global__ void combine_kernel(const T* __restrict__ x, const T* __restrict__ sh,
-                               const T* __restrict__ yp, const int* __restrict__ pos, int d, int k,
+// rounding at the end (yp rows already carry their routing weight).  On the
+// tensor-core path the shared expert's output sh is fp32 (ST) and the
+// weighted rows yp fp16 (YT); elsewhere both are the handle dtype.
+template <typename T, typename YT = T, typename ST = T>
+__global__ void combine_kernel(const T* __restrict__ x, const ST* __restrict__ sh,
+                               const YT* __restrict__ yp, const int* __restrict__ pos, int d, int k,
                                T* __restrict__ out) {
     constexpr int V = Elem<T>::V;
     const size_t t = blockIdx.x;
@@ -588,13 +559,22 @@ __global__ void combine_kernel(const T* __restrict__ x, const T* __restrict__ sh
         float acc[V], tmp[V];
         load_vec<T>(x + t * d + v * V, acc);
         if (sh != nullptr) {
-            load_vec<T>(sh + t * d + v * V, tmp);
+            if constexpr (Elem<ST>::V == V) {
+                load_vec<ST>(sh + t * d + v * V, tmp);
+            } else {   // fp32 sh beside 16-bit x: two 16-byte loads per vector
+                static_assert(V == 2 * Elem<ST>::V, "vector widths");
+                float lo[Elem<ST>::V], hi[Elem<ST>::V];
+                load_vec<ST>(sh + t * d + v * V, lo);
+                load_vec<ST>(sh + t * d + v * V + Elem<ST>::V, hi);
+#pragma unroll
+                for (int i = 0; i < Elem<ST>::V; ++i) { tmp[i] = lo[i]; tmp[Elem<ST>::V + i] = hi[i]; }
+            }
 #pragma unroll
             for (int i = 0; i < V; ++i) acc[i] += tmp[i];
         }
         for (int j = 0; j < k; ++j) {
             const size_t row = static_cast<size_t>(pos[t * k + j]);
-            load_vec<T>(yp + row * d + v * V, tmp);
+            load_vec<YT>(yp + row * d + v * V, tmp);
 #pragma unroll
             for (int i = 0; i < V; ++i) acc[i] += tmp[i];
         }
@@ -622,6 +602,62 @@ __global__ void splitk_residual_kernel(const float* __restrict__ part, int nspli
         out[4 * i + 1] = Elem<T>::from_f(acc.y + r[1]);
         out[4 * i + 2] = Elem<T>::from_f(acc.z + r[2]);
         out[4 * i + 3] = Elem<T>::from_f(acc.w + r[3]);
+    }
+}
+
+// The query compression's split-K epilogue, one block per token: c = the sum
+// of the k-range partials part[s][t] (s in order) rounded once to the
+// storage dtype (the Linear's output), then q = gain * cast(c * r) with r the
+// reciprocal RMS of the rounded c (GlmMoeDsaRMSNorm, the same arithmetic as
+// rmsnorm_kernel).  Both passes run over 16-byte vectors; the second re-reads
+// c from memory it just wrote (L2).  rank is a multiple of the vector width.
+template <typename T>
+__global__ void splitk_rmsnorm_kernel(const float* __restrict__ part, int nsplit, size_t stride, int rank,
+                                      const T* __restrict__ gain, float eps, T* __restrict__ c_out,
+                                      T* __restrict__ q_out) {
+    __shared__ float2 red[33];
+    constexpr int V = Elem<T>::V;
+    const size_t t = blockIdx.x;
+    const float* pr = part + t * rank;
+    T* cr = c_out + t * rank;
+    float hi = 0.f, lo = 0.f;
+    for (int v = threadIdx.x; v < rank / V; v += blockDim.x) {
+        float a[V];
+#pragma unroll
+        for (int i = 0; i < V; i += 4) {
+            const float4 p4 = *reinterpret_cast<const float4*>(pr + v * V + i);
+            a[i] = p4.x; a[i + 1] = p4.y; a[i + 2] = p4.z; a[i + 3] = p4.w;
+        }
+        for (int sp = 1; sp < nsplit; ++sp) {
+#pragma unroll
+            for (int i = 0; i < V; i += 4) {
+                const float4 p4 = *reinterpret_cast<const float4*>(pr + sp * stride + v * V + i);
+                a[i] += p4.x; a[i + 1] += p4.y; a[i + 2] += p4.z; a[i + 3] += p4.w;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            a[i] = Elem<T>::round_io(a[i]);
+            const float sq = __fmul_rn(a[i], a[i]);
+            const float sqe = fmaf(a[i], a[i], -sq);
+            float s2, e2;
+            two_sum_f(hi, sq, s2, e2);
+            hi = s2;
+            lo = __fadd_rn(lo, __fadd_rn(e2, sqe));
+        }
+        store_vec<T>(cr + v * V, a);
+    }
+    block_sum_pair(hi, lo, red);   // its barriers also order the c stores before the reads below
+    const float ms = static_cast<float>((static_cast<double>(hi) + static_cast<double>(lo)) /
+                                        static_cast<double>(rank));
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+    for (int v = threadIdx.x; v < rank / V; v += blockDim.x) {
+        float f[V], g[V];
+        load_vec<T>(cr + v * V, f);
+        load_vec<T>(gain + v * V, g);
+#pragma unroll
+        for (int i = 0; i < V; ++i) f[i] = __fmul_rn(g[i], Elem<T>::round_io(__fmul_rn(f[i], r)));
+        store_vec<T>(q_out + t * rank + v * V, f);
     }
 }
 

@@ -287,29 +287,36 @@ cudaError_t run_tc(const TcParams& prm, bool pair, int P, int num_sms, cudaStrea
     return launch_tc<64, 8, EPI>(prm, grid, st);
 }
 
-template <int EPL>
-void launch_topk_e(const float2* part, const float* bias, int T, int E, int k, float scale,
-                   float* logits, int* idx, float* w, int* chunk_cnt, cudaStream_t st) {
+// Top-k from either logit source (LogitsFromPairs / LogitsPlain).  A chunk
+// of 128 tokens (one histogram) is split over up to 4 blocks until the grid
+// covers the SMs; each block takes as many warps as its registers allow, up
+// to one per token.
+template <int EPL, typename Src>
+void launch_topk_e(const Src& src, const float* bias, int T, int E, int k, float scale, int* idx,
+                   float* w, int* chunk_cnt, int num_sms, cudaStream_t st) {
     const int n_chunks = (T + CHUNK_TOKENS - 1) / CHUNK_TOKENS;
-    // one block per 128-token chunk (its histogram): the chunk count is small next to
-    // the SM count, so each block takes as many warps as its registers allow (up to 32)
+    int split = 1;
+    while (split < 4 && n_chunks * split * 2 <= num_sms) split *= 2;
     static int threads[64] = {};  // per device, found before the first launch
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) dev = 0;
     if (threads[dev] == 0) {
         cudaFuncAttributes fa;
         int tmax = 512;
-        if (cudaFuncGetAttributes(&fa, topk_kernel<EPL>) == cudaSuccess)
+        if (cudaFuncGetAttributes(&fa, topk_kernel<EPL, Src>) == cudaSuccess)
             tmax = std::min(1024, fa.maxThreadsPerBlock) / 32 * 32;
         threads[dev] = std::max(32, tmax);
     }
-    topk_kernel<EPL><<<n_chunks, threads[dev], E * sizeof(int), st>>>(part, bias, T, E, k, scale, logits,
-                                                                      idx, w, chunk_cnt);
+    const int nthreads = std::min(threads[dev], 32 * (CHUNK_TOKENS / split));
+    if (split > 1) cudaMemsetAsync(chunk_cnt, 0, static_cast<size_t>(n_chunks) * E * sizeof(int), st);
+    topk_kernel<EPL, Src><<<n_chunks * split, nthreads, E * sizeof(int), st>>>(src, bias, T, E, k, scale, idx, w,
+                                                                               chunk_cnt, split);
 }
 
-void launch_topk(const float2* part, const float* bias, int T, int E, int k, float scale,
-                 float* logits, int* idx, float* w, int* chunk_cnt, cudaStream_t st) {
-#define MOE_TOPK(EPL) launch_topk_e<EPL>(part, bias, T, E, k, scale, logits, idx, w, chunk_cnt, st)
+template <typename Src>
+void launch_topk(const Src& src, const float* bias, int T, int E, int k, float scale, int* idx, float* w,
+                 int* chunk_cnt, int num_sms, cudaStream_t st) {
+#define MOE_TOPK(EPL) launch_topk_e<EPL>(src, bias, T, E, k, scale, idx, w, chunk_cnt, num_sms, st)
     if (E <= 32) MOE_TOPK(1);
     else if (E <= 64) MOE_TOPK(2);
     else if (E <= 128) MOE_TOPK(4);
@@ -380,7 +387,7 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     if (h->tc) {
         // a warp per token once there are enough tokens to fill the SMs; small
         // batches (decode) keep a whole block on each token
-        if (d / Elem<T>::V <= 32 * RMS_WARP_VECS && Tn >= 8 * h->num_sms)
+        if (Tn >= 8 * h->num_sms)
             rmsnorm_warp_kernel<T><<<(Tn + 7) / 8, 256, 0, st>>>(x, static_cast<const T*>(a.norm_w), xn, Tn,
                                                                  d, c.eps);
         else
@@ -398,8 +405,8 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     }
     // C+D: top-k, weights, chunk histograms; E: scan, scatter, gather
     mark(h, 2, st);
-    launch_topk(h->part, a.bias, Tn, E, k, a.scale, h->logits, h->topk_idx, h->topk_w, h->chunk_cnt,
-                st);
+    launch_topk(LogitsFromPairs{h->part, h->logits}, a.bias, Tn, E, k, a.scale, h->topk_idx, h->topk_w,
+                h->chunk_cnt, h->num_sms, st);
     mark(h, 3, st);
     scan_kernel<<<1, std::max(32, (E + 31) / 32 * 32), 0, st>>>(h->chunk_cnt, n_chunks, E,
                                                                h->counts, h->offsets, h->chunk_base);
@@ -407,6 +414,9 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     scatter_kernel<<<n_chunks, CHUNK_TOKENS, E * (CHUNK_TOKENS / 32) * sizeof(uint32_t), st>>>(
         h->topk_idx, h->topk_w, Tn, E, k, h->chunk_base, h->pos, h->row_tok, h->row_w);
     mark(h, 5, st);
+    // CTA pairs (256 x 256 tiles) once experts average 64 tokens or more; below
+    // that the single-CTA kernel with 64-token tiles wastes less.
+    const bool pair = h->tc && P >= 64 * E;
     if (Tn >= 8 * h->num_sms)   // a warp per token: each xn row read once
         gather_tokens_kernel<T><<<std::min(8 * h->num_sms, (Tn + 7) / 8), 256, 0, st>>>(
             xn, h->pos, static_cast<T*>(h->xp), Tn, k, d, P);
@@ -421,10 +431,8 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     T* hs = static_cast<T*>(h->hs);
     T* sh = Is > 0 ? static_cast<T*>(h->sh) : nullptr;
     if (h->tc) {
-        // CTA pairs (256 x 256 tiles) once experts average 64 tokens or more;
-        // below that the single-CTA kernel with 64-token tiles wastes less.
-        const bool pair = P >= 64 * E;
-        // F+H(gate/up): routed + shared gate|up with SwiGLU epilogue
+        auto fail = [&]() { return MOE_ERR_CUDA; };
+        // F+H(gate|up): routed + shared gate|up with the SwiGLU epilogue, one launch
         TcParams g1;
         std::memset(&g1, 0, sizeof g1);
         g1.E = E;
@@ -436,25 +444,26 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
             // gate and up halves of 64 features in one copy: {f < I, k, half (stride I), expert}
             if (!map_4d_chunks(&g1.a0[0], a.gate_up, I, d, I2 * 2, 2, uint64_t(I) * 2, E, d * I2 * 2) ||
                 !map_2d(&g1.b[0], h->xp, d, P) || !map_2d(&g1.b128[0], h->xp, d, P, 128))
-                return MOE_ERR_CUDA;
+                return fail();
             g1.seg[0] = TcSeg{1, 0, d, 128, I, (I + 127) / 128, I, I, hbuf, nullptr, 64, PA_HALVES_4D};
         } else {
             if (!map_3d(&g1.a0[0], a.gate_up, I2, d, E) || !map_3d(&g1.a1[0], a.gate_up, I2, d, E) ||
                 !map_2d(&g1.b[0], h->xp, d, P))
-                return MOE_ERR_CUDA;
+                return fail();
             g1.seg[0] = TcSeg{1, 0, d, 64, I, I / 64, I, I, hbuf, nullptr, 0, 0};
         }
         if (Is > 0) {
             if (!map_2d(&g1.a0[1], a.sg, d, Is) || !map_2d(&g1.a1[1], a.su, d, Is) ||
                 !map_2d(&g1.b[1], xn, d, Tn) || !map_2d(&g1.b128[1], xn, d, Tn, 128))
-                return MOE_ERR_CUDA;
+                return fail();
             g1.seg[1] = pair ? TcSeg{0, Tn, d, 128, 0, (Is + 127) / 128, Is, Is, hs, nullptr, 64, PA_TWO_2D}
                              : TcSeg{0, Tn, d, 64, 0, Is / 64, Is, Is, hs, nullptr, 0, 0};
             set_dense_groups(g1.seg[1], pair ? 256 : 128);
         }
-        if (run_tc<EPI_SWIGLU>(g1, pair, P, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        if (run_tc<EPI_SWIGLU>(g1, pair, P, h->num_sms, st) != cudaSuccess) return fail();
         mark(h, 7, st);
-        // G+H(down): routed down with routing weight + shared down
+        // G+H(down): routed down projection with the routing weight -> yp (fp16),
+        // and the shared expert's down projection -> sh (fp32), one launch
         TcParams g2;
         std::memset(&g2, 0, sizeof g2);
         g2.E = E;
@@ -466,32 +475,46 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
             if (!map_4d_chunks(&g2.a0[0], a.down, 64, I, uint64_t(d) * 2, d / 64, 128, E,
                                uint64_t(I) * d * 2) ||
                 !map_2d(&g2.b[0], hbuf, I, P) || !map_2d(&g2.b128[0], hbuf, I, P, 128))
-                return MOE_ERR_CUDA;
+                return fail();
             g2.seg[0] = TcSeg{1, 0, I, 256, 64, (d + 255) / 256, d, d, yp, h->row_w, 128, PA_CHUNKS_4D};
         } else {
             if (!map_3d(&g2.a0[0], a.down, d, I, E) || !map_3d(&g2.a1[0], a.down, d, I, E) ||
                 !map_2d(&g2.b[0], hbuf, I, P))
-                return MOE_ERR_CUDA;
+                return fail();
             g2.seg[0] = TcSeg{1, 0, I, 128, 64, (d + 127) / 128, d, d, yp, h->row_w, 0, 0};
         }
+        // the weighted rows go to the combine in fp16: the same bytes as bf16,
+        // with 3 more significand bits (an overflow is reported as MOE_ERR_RANGE)
+        g2.seg[0].out_kind = OUT_F16;
         if (Is > 0) {
             if (pair) {
                 // 128 consecutive nn.Linear rows of the shared down projection in one copy
                 if (!map_2d(&g2.a0[1], a.sd, Is, d, 128) || !map_2d(&g2.b[1], hs, Is, Tn) ||
                     !map_2d(&g2.b128[1], hs, Is, Tn, 128))
-                    return MOE_ERR_CUDA;
-                g2.seg[1] = TcSeg{0, Tn, Is, 256, 64, (d + 255) / 256, d, d, sh, nullptr, 128, PA_ONE_2D};
+                    return fail();
+                g2.seg[1] = TcSeg{0, Tn, Is, 256, 64, (d + 255) / 256, d, d, h->sh, nullptr, 128, PA_ONE_2D};
                 set_dense_groups(g2.seg[1], 256);
             } else {
                 if (!map_2d(&g2.a0[1], a.sd, Is, d) || !map_2d(&g2.a1[1], a.sd, Is, d) ||
                     !map_2d(&g2.b[1], hs, Is, Tn))
-                    return MOE_ERR_CUDA;
-                g2.seg[1] = TcSeg{0, Tn, Is, 128, 64, (d + 127) / 128, d, d, sh, nullptr, 0, 0};
+                    return fail();
+                g2.seg[1] = TcSeg{0, Tn, Is, 128, 64, (d + 127) / 128, d, d, h->sh, nullptr, 0, 0};
                 set_dense_groups(g2.seg[1], 128);
             }
+            // the shared expert's output reaches the combine in fp32, never rounded on its own
+            g2.seg[1].out_kind = OUT_F32;
         }
-        if (run_tc<EPI_WEIGHTED>(g2, pair, P, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        if (run_tc<EPI_WEIGHTED>(g2, pair, P, h->num_sms, st) != cudaSuccess) return fail();
         h->launches += 2;
+        // I: combine with the residual
+        mark(h, 8, st);
+        if constexpr (std::is_same<T, __nv_bfloat16>::value)   // the tensor-core path stores bf16
+            combine_kernel<T, __half, float><<<Tn, 256, 0, st>>>(x, Is > 0 ? static_cast<const float*>(h->sh) : nullptr,
+                                                                 static_cast<const __half*>(h->yp), h->pos, d, k,
+                                                                 static_cast<T*>(a.out));
+        h->launches += 1;
+        mark(h, moe_handle::NSTAGE, st);
+        return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
     } else {
         const T* gu = static_cast<const T*>(a.gate_up);
         const T* dn = static_cast<const T*>(a.down);
@@ -527,7 +550,7 @@ moe_status dense_impl(moe_handle* h, int Tn, const void* x_, const void* norm_w,
     const T* x = static_cast<const T*>(x_);
     T* xn = static_cast<T*>(h->xn);
     T* hd = static_cast<T*>(h->hd);
-    if (d / Elem<T>::V <= 32 * RMS_WARP_VECS && Tn >= 8 * h->num_sms)
+    if (Tn >= 8 * h->num_sms)
         rmsnorm_warp_kernel<T><<<(Tn + 7) / 8, 256, 0, st>>>(x, static_cast<const T*>(norm_w), xn, Tn, d,
                                                              c.eps);
     else
@@ -589,6 +612,78 @@ moe_status dense_impl(moe_handle* h, int Tn, const void* x_, const void* norm_w,
             hd, static_cast<const T*>(dw), Id, d, static_cast<T*>(out), x);
         h->launches += 3;
     }
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Query compression of the sparse latent attention: c = hidden · w_qaᵀ (the
+// Linear's output, rounded once to the storage dtype), q = RMSNorm(c).
+// Prefill-sized batches run the CTA-pair GEMM with a plain epilogue, then the
+// RMSNorm over the rank features of c.  Small batches run the single-CTA GEMM
+// split over k-ranges (enough tiles to stream w_qa with every SM) and one
+// kernel that adds the partials, rounds c and normalises it.
+template <typename T>
+moe_status q_latent_impl(moe_handle* h, int Tn, int rank, const void* hidden, const void* w_qa,
+                         const void* gain, void* c_out, void* q_out, cudaStream_t st) {
+    const moe_config& c = h->cfg;
+    const int d = c.hidden;
+    T* cq = static_cast<T*>(c_out);
+    auto norm = [&]() {
+        if (Tn >= 8 * h->num_sms)
+            rmsnorm_warp_kernel<T><<<(Tn + 7) / 8, 256, 0, st>>>(cq, static_cast<const T*>(gain),
+                                                                 static_cast<T*>(q_out), Tn, rank, c.eps);
+        else
+            rmsnorm_kernel<T><<<Tn, 256, 0, st>>>(cq, static_cast<const T*>(gain), static_cast<T*>(q_out),
+                                                  rank, c.eps);
+    };
+    if (!h->tc) {
+        simt_shared_down_kernel<T><<<dim3(Tn, (rank + 127) / 128), 128, d * sizeof(float), st>>>(
+            static_cast<const T*>(hidden), static_cast<const T*>(w_qa), d, rank, cq);
+        norm();
+        h->launches += 2;
+        return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
+    TcParams g;
+    std::memset(&g, 0, sizeof g);
+    g.E = 1;
+    g.offsets = h->offsets;
+    g.err = h->err;
+    g.n_segs = 1;
+    const int tiles_pair = ((Tn + 255) / 256) * ((rank + 255) / 256);
+    const bool pair = Tn >= 128 && 2 * tiles_pair >= h->num_sms;
+    if (pair) {
+        if (!map_2d(&g.a0[0], w_qa, d, rank, 128) || !map_2d(&g.b[0], hidden, d, Tn) ||
+            !map_2d(&g.b128[0], hidden, d, Tn, 128))
+            return MOE_ERR_CUDA;
+        g.seg[0] = TcSeg{0, Tn, d, 256, 64, (rank + 255) / 256, rank, rank, c_out, nullptr, 128, PA_ONE_2D};
+        set_dense_groups(g.seg[0], 256);
+        if (run_tc<EPI_WEIGHTED>(g, true, Tn, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        norm();
+        h->launches += 2;
+        return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
+    if (!map_2d(&g.a0[0], w_qa, d, rank) || !map_2d(&g.a1[0], w_qa, d, rank) || !map_2d(&g.b[0], hidden, d, Tn))
+        return MOE_ERR_CUDA;
+    g.seg[0] = TcSeg{0, Tn, d, 128, 64, (rank + 127) / 128, rank, rank, c_out, nullptr, 0, 0};
+    set_dense_groups(g.seg[0], 128);
+    const int tiles = ((Tn + 63) / 64) * ((rank + 127) / 128);
+    // the split-K partials [ks][Tn][rank] must fit the handle's buffer [8][min(T, 128)][d]
+    const int ks = Tn <= std::min(c.max_tokens, DENSE_SPLIT_MAX_T) && rank <= d
+                       ? std::max(1, std::min({d / 64, DENSE_SPLIT_MAX, h->num_sms / tiles}))
+                       : 1;
+    const int grid_cap = h->num_sms;
+    if (ks > 1) {
+        g.seg[0].out = h->dpart;
+        g.seg[0].k_split = ks;
+        const int grid = std::max(1, std::min(grid_cap, tile_bound(g, 64, Tn)));
+        if (launch_tc<64, 8, EPI_PARTIAL>(g, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+        splitk_rmsnorm_kernel<T><<<Tn, 256, 0, st>>>(h->dpart, ks, static_cast<size_t>(Tn) * rank, rank,
+                                                     static_cast<const T*>(gain), c.eps, cq,
+                                                     static_cast<T*>(q_out));
+    } else {
+        if (run_tc<EPI_WEIGHTED>(g, false, Tn, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        norm();
+    }
+    h->launches += 2;
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -674,13 +769,6 @@ int* route_scratch(int dev) {
     return g_route_scratch_dev[dev];
 }
 
-template <int EPL>
-void launch_topk_logits_e(const float* logits, const float* bias, int T, int E, int k, float scale,
-                          int* idx, float* w, int* chunk_cnt, cudaStream_t st) {
-    const int n_chunks = (T + CHUNK_TOKENS - 1) / CHUNK_TOKENS;
-    topk_logits_kernel<EPL><<<n_chunks, 512, E * sizeof(int), st>>>(logits, bias, T, E, k, scale,
-                                                                    idx, w, chunk_cnt);
-}
 }  // namespace
 
 extern "C" {
@@ -698,6 +786,15 @@ moe_status moe_route_static(int32_t T, int32_t E, int32_t top_k, float routed_sc
     const void* ptrs[] = {logits, corr_bias, idx, w, counts, offsets, pos, row_tok, row_w};
     for (const void* p : ptrs)
         if (p == nullptr || (reinterpret_cast<uintptr_t>(p) & 3u) != 0) return MOE_ERR_INVALID_ARG;
+    // no output may overlap an input or another output
+    const size_t Tk = static_cast<size_t>(T) * top_k * 4, Eb = static_cast<size_t>(E) * 4;
+    const struct { const void* p; size_t n; } bufs[] = {
+        {logits, static_cast<size_t>(T) * Eb}, {corr_bias, Eb}, {idx, Tk}, {w, Tk}, {counts, Eb},
+        {offsets, Eb + 4}, {pos, Tk}, {row_tok, Tk}, {row_w, Tk}};
+    constexpr int n_bufs = sizeof(bufs) / sizeof(bufs[0]);
+    for (int o = 2; o < n_bufs; ++o)
+        for (int i = 0; i < n_bufs; ++i)
+            if (i != o && overlaps(bufs[o].p, bufs[o].n, bufs[i].p, bufs[i].n)) return MOE_ERR_INVALID_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
     int* scratch = route_scratch(dev);
@@ -706,15 +803,9 @@ moe_status moe_route_static(int32_t T, int32_t E, int32_t top_k, float routed_sc
     int* chunk_base = scratch + ROUTE_STATIC_MAX_CELLS;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int nch = static_cast<int>(n_chunks);
-#define MOE_TOPK_LOGITS(EPL) \
-    launch_topk_logits_e<EPL>(logits, corr_bias, T, E, top_k, routed_scale, idx, w, chunk_cnt, st)
-    if (E <= 32) MOE_TOPK_LOGITS(1);
-    else if (E <= 64) MOE_TOPK_LOGITS(2);
-    else if (E <= 128) MOE_TOPK_LOGITS(4);
-    else if (E <= 256) MOE_TOPK_LOGITS(8);
-    else if (E <= 512) MOE_TOPK_LOGITS(16);
-    else MOE_TOPK_LOGITS(32);
-#undef MOE_TOPK_LOGITS
+    int n_sms = 148;
+    if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+    launch_topk(LogitsPlain{logits}, corr_bias, T, E, top_k, routed_scale, idx, w, chunk_cnt, n_sms, st);
     scan_kernel<<<1, std::max(32, (E + 31) / 32 * 32), 0, st>>>(chunk_cnt, nch, E, counts, offsets,
                                                                chunk_base);
     scatter_kernel<<<nch, CHUNK_TOKENS, E * (CHUNK_TOKENS / 32) * sizeof(uint32_t), st>>>(
@@ -772,6 +863,7 @@ const char* moe_status_string(moe_status s) {
         case MOE_ERR_CUDA: return "CUDA error";
         case MOE_ERR_OOM: return "out of device memory";
         case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+        case MOE_ERR_RANGE: return "a weighted expert row exceeded the fp16 range of its intermediate";
     }
     return "unknown status";
 }
@@ -845,11 +937,10 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out) {
     alloc(&h->h, P * I * es);
     alloc(&h->yp, P * d * es);
     alloc(&h->hs, T * std::max<size_t>(Is, 1) * es);
-    alloc(&h->sh, T * d * es);
-    if (c.dense_inter > 0) {
-        alloc(&h->hd, T * static_cast<size_t>(c.dense_inter) * es);
-        if (tc) alloc(&h->dpart, static_cast<size_t>(DENSE_SPLIT_MAX) * std::min<size_t>(T, DENSE_SPLIT_MAX_T) * d * 4);
-    }
+    alloc(&h->sh, T * d * (tc ? 4 : es));   // the tensor-core path keeps the shared expert's output in fp32
+    if (c.dense_inter > 0) alloc(&h->hd, T * static_cast<size_t>(c.dense_inter) * es);
+    // split-K partials of the dense down projection and of the query compression
+    if (tc) alloc(&h->dpart, static_cast<size_t>(DENSE_SPLIT_MAX) * std::min<size_t>(T, DENSE_SPLIT_MAX_T) * d * 4);
     if (!dense_only) {   // host-I/O staging of moe_forward_host(_async)
         alloc(&h->x_stage, T * d * es);
         alloc(&h->out_stage, T * d * es);
@@ -913,6 +1004,31 @@ moe_status moe_dense_forward(moe_handle* h, int32_t T, const void* x, const void
     return c.dtype == MOE_DTYPE_BF16
                ? dense_impl<__nv_bfloat16>(h, T, x, norm_w, gate_w, up_w, down_w, inter, out, st)
                : dense_impl<float>(h, T, x, norm_w, gate_w, up_w, down_w, inter, out, st);
+}
+
+moe_status moe_q_latent(moe_handle* h, int32_t T, int32_t q_rank, const void* hidden, const void* w_qa,
+                        const void* q_norm_w, void* c_out, void* q_out, void* stream) {
+    if (!h) return MOE_ERR_INVALID_ARG;
+    const moe_config& c = h->cfg;
+    if (T < 0 || q_rank < 1) return MOE_ERR_INVALID_ARG;
+    if (q_rank % (h->tc ? 64 : 16 / h->es) != 0) return MOE_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(T) * std::max(q_rank, c.hidden) > (int64_t(1) << 31) - 1) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;  // nothing is read or written
+    const void* ptrs[] = {hidden, w_qa, q_norm_w, c_out, q_out};
+    for (const void* p : ptrs)
+        if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    const size_t es = h->es, d = c.hidden, R = q_rank;
+    const size_t nc = static_cast<size_t>(T) * R * es;
+    const struct { const void* p; size_t n; } bufs[] = {
+        {hidden, static_cast<size_t>(T) * d * es}, {w_qa, R * d * es}, {q_norm_w, R * es}};
+    for (const auto& in : bufs)
+        if (overlaps(c_out, nc, in.p, in.n) || overlaps(q_out, nc, in.p, in.n)) return MOE_ERR_INVALID_ARG;
+    if (overlaps(c_out, nc, q_out, nc)) return MOE_ERR_INVALID_ARG;
+    if (cudaSetDevice(c.device) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return c.dtype == MOE_DTYPE_BF16
+               ? q_latent_impl<__nv_bfloat16>(h, T, q_rank, hidden, w_qa, q_norm_w, c_out, q_out, st)
+               : q_latent_impl<float>(h, T, q_rank, hidden, w_qa, q_norm_w, c_out, q_out, st);
 }
 
 moe_status moe_forward_host(moe_handle* h, int32_t T, const void* x_host, const void* norm_w,
@@ -1018,7 +1134,7 @@ moe_status moe_get_intermediate(moe_handle* h, moe_tensor which, void* dst, size
         case MOE_T_POS: src = h->pos; bytes = T * k * 4; break;
         case MOE_T_ROW_TOK: src = h->row_tok; bytes = T * k * 4; break;
         case MOE_T_H: src = h->h; bytes = T * k * h->cfg.inter * h->es; break;
-        case MOE_T_SHARED: src = h->sh; bytes = h->cfg.shared_inter > 0 ? T * d * h->es : 0; break;
+        case MOE_T_YP: src = h->yp; bytes = T * k * d * h->es; break;
         default: return MOE_ERR_INVALID_ARG;
     }
     if (dst_bytes < bytes) return MOE_ERR_INVALID_ARG;
@@ -1038,7 +1154,7 @@ moe_status moe_sync_status(moe_handle* h, void* stream) {
     if (cudaMemcpy(&flag, h->err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
     if (flag != 0) {
         if (cudaMemset(h->err, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
-        return MOE_ERR_TIMEOUT;
+        return (flag & DEVERR_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_ERR_RANGE;
     }
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

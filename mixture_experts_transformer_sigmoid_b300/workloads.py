@@ -15,7 +15,7 @@ same weight shapes share the same weights, e.g. GLM-5 prefill and decode):
 
   tensor index:  x=0, norm_w=1, router_w=2, corr_bias=3, gate_up=4, down=5,
                  shared_gate=6, shared_up=7, shared_down=8, hot_experts=9,
-                 dense_gate=10, dense_up=11, dense_down=12
+                 dense_gate=10, dense_up=11, dense_down=12, w_qa=13, q_norm_w=14
   generator seed: seed * 16 + tensor index
 
   x ~ N(0, 1); norm_w ~ U(0.5, 1.5); all projection weights ~ N(0, 0.02);
@@ -29,6 +29,10 @@ its RMSNorm and residual) has workloads of its own (``DENSE_WORKLOADS``):
 the same x and norm_w recipe, and nn.Linear gate, up [I, d] and down [d, I]
 weights ~ N(0, 0.02).  The pages do not print GLM-5's dense intermediate
 size; the GLM-5-sized dense workloads take I = 2 d = 12288.
+
+The query compression of the sparse latent attention (``QLATENT_WORKLOADS``)
+draws hidden ~ N(0, 1) (from the x generator), w_qa ~ N(0, 0.02) [rank, d]
+and q_norm_w ~ U(0.5, 1.5).
 """
 from __future__ import annotations
 
@@ -41,6 +45,7 @@ TENSOR_INDEX = {
     "x": 0, "norm_w": 1, "router_w": 2, "corr_bias": 3, "gate_up": 4,
     "down": 5, "shared_gate": 6, "shared_up": 7, "shared_down": 8,
     "hot_experts": 9, "dense_gate": 10, "dense_up": 11, "dense_down": 12,
+    "w_qa": 13, "q_norm_w": 14,
 }
 
 
@@ -133,6 +138,57 @@ DENSE_WORKLOADS: Dict[str, DenseWorkload] = {
     "glm5_dense_decode": DenseWorkload("glm5_dense_decode", T=64, d=6144, I=12288,
                                        dtype="bf16", description="T64 d6144 I12288 bf16"),
 }
+
+
+@dataclasses.dataclass(frozen=True)
+class QLatentWorkload:
+    """The query compression of the sparse latent attention: hidden [T, d]
+    (the attention input) -> q_a_proj (w_qa [rank, d]) -> q_a_layernorm."""
+    name: str
+    T: int
+    d: int
+    rank: int               # q_lora_rank
+    dtype: str
+    eps: float = 1e-6
+    description: str = ""
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float32 if self.dtype == "fp32" else torch.bfloat16
+
+    def with_(self, **kw) -> "QLatentWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+# GLM-5: d = 6144 and q_lora_rank = 2048 (the query latent's shape on the GLM-5
+# "Query latent" page); the small cases cover both GEMM paths and ragged sizes.
+QLATENT_WORKLOADS: Dict[str, QLatentWorkload] = {
+    "q_tiny_fp32": QLatentWorkload("q_tiny_fp32", T=40, d=256, rank=64, dtype="fp32"),
+    "q_small_bf16": QLatentWorkload("q_small_bf16", T=300, d=512, rank=192, dtype="bf16"),
+    "q_pair_bf16": QLatentWorkload("q_pair_bf16", T=4800, d=1024, rank=1024, dtype="bf16"),
+    "glm5_q_prefill": QLatentWorkload("glm5_q_prefill", T=8192, d=6144, rank=2048, dtype="bf16",
+                                      description="T8192 d6144 q_lora_rank 2048 bf16"),
+    "glm5_q_decode": QLatentWorkload("glm5_q_decode", T=64, d=6144, rank=2048, dtype="bf16",
+                                     description="T64 d6144 q_lora_rank 2048 bf16"),
+}
+
+
+def make_q_inputs(w: QLatentWorkload, seed: int = 0, device: str = "cpu", T: Optional[int] = None,
+                  weights_from: Optional[Dict[str, torch.Tensor]] = None) -> Dict[str, torch.Tensor]:
+    """hidden ~ N(0, 1) (the attention input, an RMSNorm output), w_qa ~ N(0,
+    0.02) as nn.Linear [rank, d], q_norm_w ~ U(0.5, 1.5); the x, w_qa and
+    q_norm_w generators of the recipe above."""
+    T = w.T if T is None else T
+    dt = w.torch_dtype
+    out: Dict[str, torch.Tensor] = {}
+    out["hidden"] = _normal((T, w.d), 1.0, _gen(seed, "x", device), device, dt)
+    if weights_from is not None:
+        out["w_qa"], out["q_norm_w"] = weights_from["w_qa"], weights_from["q_norm_w"]
+        return out
+    out["w_qa"] = _normal((w.rank, w.d), 0.02, _gen(seed, "w_qa", device), device, dt)
+    g = _gen(seed, "q_norm_w", device)
+    out["q_norm_w"] = (torch.rand(w.rank, generator=g, device=device) + 0.5).to(dt)
+    return out
 
 
 def _gen(seed: int, name: str, device: str) -> torch.Generator:

@@ -1,21 +1,18 @@
 """Helpers shared by the GPU parity tests, the smoke check and the benchmark:
 run the CUDA path through the C ABI and compare it with the CPU oracle.
 
-Tolerances (floating point):
-  bf16 storage: |gpu - oracle| <= 2e-2 * rms(oracle) + half a bf16 ulp of the
-                oracle value, elementwise, and
+Tolerances (floating point), as stated for this sublayer:
+  bf16 storage: max|gpu - oracle| <= 2e-2 * rms(oracle)  and
                 sum|gpu - oracle| / sum|oracle| <= 5e-3
   fp32 storage: max|gpu - oracle| <= 1e-4 * rms(oracle)
-The half ulp is the output's own rounding to bf16 (up to 2^-8 |out|), which
-the stored dtype makes unavoidable: on its own it exceeds 2e-2 * rms(oracle)
-wherever |out| > 5.12 rms(oracle), and the tail of a few hundred thousand
-outputs reaches that range.  The plain max|gpu - oracle| / rms(oracle) is
-reported beside it.
+The oracle's output is fp64 rounded to fp32; the GPU's is the stored dtype.
 Routing: expert ids are compared exactly; a token may differ only when its
 top-k margin b_(k) - b_(k+1) is below 1e-5 (several selections are then
-correct) or when its RMSNorm output differs in some bf16 rounding from the
-oracle's.  Output parity is judged against the oracle run on the GPU's own
-selection, so a correct alternative selection is not counted as an error.
+correct), or when its RMSNorm output differs from the oracle's in a bf16
+rounding whose effect on the biased scores can reach that token's margin
+(bounded by the router weights; see check_end_to_end_routing).  Output
+parity is judged against the oracle run on the GPU's own selection, so a
+correct alternative selection is not counted as an error.
 """
 from __future__ import annotations
 
@@ -164,19 +161,12 @@ def output_errors(gpu, ref):
             "mean_rel": float(diff.sum() / max(np.abs(ref).sum(), 1e-30))}
 
 
-def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
-    """Half the spacing of bf16 values (8 significant bits) around |v|."""
-    a = np.abs(v.astype(np.float64))
-    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
-    return np.where(a > 0, 2.0 ** (e - 8), 0.0)
-
-
 def check_bf16_max(gpu, ref, max_rms):
-    """Elementwise |gpu - ref| <= max_rms * rms(ref) + half_ulp_bf16(ref)."""
+    """max|gpu - ref| <= max_rms * rms(ref) over every compared element."""
     ref64 = ref.astype(np.float64)
     rms = float(np.sqrt(np.mean(ref64 ** 2)))
-    excess = np.abs(gpu.astype(np.float64) - ref64) - (max_rms * rms + half_ulp_bf16(ref64))
-    assert excess.max(initial=-1.0) <= 0.0, f"bf16 output error above the bound by {float(excess.max())}"
+    err = float(np.abs(gpu.astype(np.float64) - ref64).max(initial=0.0))
+    assert err <= max_rms * rms, f"bf16 output error {err / rms:.5f} * rms(oracle) > {max_rms}"
 
 
 def check_output(g, host, c, dtype, rows=None):
@@ -198,14 +188,36 @@ def check_output(g, host, c, dtype, rows=None):
     return {"out": st, "delta": sd}
 
 
+def flip_reach(g_xn, o_xn, router_w):
+    """Per token: an upper bound of how far the GPU's and the oracle's
+    biased-score gap between any two experts can move because their RMSNorm
+    outputs differ.  |dl_e| <= sum_j |dxn_j| |Wr[e, j]|, the sigmoid's slope
+    is at most 1/4, and two experts' scores can move towards each other, so
+    the reach is 2 * (max_e |dl_e| / 4 + the router's own logit error / 4)."""
+    wr = ((router_w.astype(np.uint32) << 16).view(np.float32) if router_w.dtype == np.uint16
+          else router_w.astype(np.float32))
+    dxn = np.abs(g_xn.astype(np.float64) - o_xn.astype(np.float64))
+    dl = dxn @ np.abs(wr.astype(np.float64)).T
+    return 2.0 * (dl.max(axis=1) / 4.0 + LOGIT_ABS_TOL / 4.0)
+
+
 def check_end_to_end_routing(g, host, c, rows):
     """Oracle's own routing (its own xn) against the GPU's, for the sampled
-    rows: a difference must be a near-tie or follow an xn rounding flip."""
+    rows.  A difference must be a near-tie (margin < 1e-5) or a token whose
+    RMSNorm output differs from the oracle's by enough to reach its margin
+    (flip_reach >= margin); both are counted and reported apart."""
     r = orc.forward(c, host, rows=np.asarray(rows))
     gi = g["idx"][rows]
     mismatch = np.any(np.sort(gi, axis=1) != np.sort(r["idx"], axis=1), axis=1)
-    xn_flip = np.any(g["xn"][rows] != r["xn"], axis=1)
-    unexplained = mismatch & (r["margin"] >= NEAR_TIE) & ~xn_flip
+    near_tie = r["margin"] < NEAR_TIE
+    xn_diff = np.any(g["xn"][rows] != r["xn"], axis=1)
+    reach = np.zeros(len(rows))
+    cand = mismatch & ~near_tie & xn_diff
+    if cand.any():
+        reach[cand] = flip_reach(g["xn"][rows][cand], r["xn"][cand], host["router_w"])
+    excused_flip = cand & (reach >= r["margin"])
+    unexplained = mismatch & ~near_tie & ~excused_flip
     assert not unexplained.any(), f"{int(unexplained.sum())} unexplained routing differences"
-    return {"mismatch": int(mismatch.sum()), "near_tie": int((r["margin"] < NEAR_TIE).sum()),
-            "xn_rows_differ": int(xn_flip.sum())}
+    return {"mismatch": int(mismatch.sum()), "near_tie": int(near_tie.sum()),
+            "near_tie_mismatch": int((mismatch & near_tie).sum()),
+            "xn_flip_excused": int(excused_flip.sum()), "xn_rows_differ": int(xn_diff.sum())}

@@ -142,6 +142,21 @@ def test_route_static_host_checks(lib, T, E, k, status):
     assert lib.moe_route_static(T, E, k, 1.0, *nulls, None) == status
 
 
+def test_route_static_rejects_overlap_before_touching_the_device(lib):
+    """Outputs overlapping an input or each other are rejected by the host
+    checks, before any CUDA call (fake, aligned addresses: nothing is read)."""
+    T, E, k = 256, 16, 2                        # logits 16 KB, each [T, k] array 2 KB
+    base = [ctypes.c_void_p((i + 1) << 20) for i in range(9)]
+    logits, bias, idx, w, counts, offsets, pos, row_tok, row_w = base
+    over_logits = ctypes.c_void_p((1 << 20) + 4096)
+    assert lib.moe_route_static(T, E, k, 1.0, logits, bias, idx, over_logits, counts, offsets, pos,
+                                row_tok, row_w, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_static(T, E, k, 1.0, logits, bias, idx, w, counts, offsets, pos,
+                                ctypes.c_void_p((7 << 20) + 1024), row_w, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_static(T, E, k, 1.0, logits, bias, idx, w, bias, offsets, pos,
+                                row_tok, row_w, None) == B.MOE_ERR_INVALID_ARG
+
+
 def test_host_io_entry_points_reject_a_null_handle(lib):
     nulls = [None] * 11
     assert lib.moe_forward_host_async(None, 4, *nulls[:9], 2, 1.0, None, None) == B.MOE_ERR_INVALID_ARG

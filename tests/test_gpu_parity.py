@@ -151,7 +151,9 @@ def test_aliasing_output_rejected():
 
 
 # ---------------------------------------------------------------- workloads
-SAMPLE = {"small_bf16": 256, "air_prefill": 96, "glm5_prefill": 24, "glm5_decode": 64}
+# Output parity on a fixed seeded sample of tokens (the oracle runs at about 70
+# tokens/s on the GLM-5 shapes); routing is compared on every token.
+SAMPLE = {"small_bf16": 2048, "air_prefill": 512, "glm5_prefill": 1024, "glm5_decode": 64}
 
 
 def workload_check(name, dev_gen):

@@ -13,12 +13,15 @@ second reads the shared scratch right after the first left its own
 contents there.  This file sorts last so that a run stopping at the first
 failure has run every other test before it.
 """
+import numpy as np
 import pytest
 import torch
 
+import parity
 from mixture_experts_transformer_sigmoid_b300 import binding as B
 from mixture_experts_transformer_sigmoid_b300 import build as build_mod
 from mixture_experts_transformer_sigmoid_b300 import workloads as wl
+from oracle import oracle as orc
 
 pytestmark = pytest.mark.gpu
 
@@ -73,3 +76,40 @@ def test_route_static_rejects_sizes_beyond_its_scratch():
     with pytest.raises(B.MoeError) as ei:
         B.route_static(logits, bias, 8, 1.0)
     assert ei.value.status == B.MOE_ERR_UNSUPPORTED
+
+
+def test_route_static_matches_oracle_selection():
+    """The selection and weights against the oracle's steps C-D run on the
+    same fp32 logits: the same set of experts per token (a k-th / (k+1)-th
+    margin below 1e-5 excepted), an order the scores allow, and weights
+    within 2e-6 relative."""
+    T, E, k, scale = 1000, 96, 6, 2.5
+    g = torch.Generator().manual_seed(11)
+    logits = torch.randn((T, E), generator=g) * 1.5
+    bias = (torch.rand(E, generator=g) * 2 - 1) * 0.05
+    got = B.route_static(logits.cuda(), bias.cuda(), k, scale)
+    torch.cuda.synchronize()
+    c = orc.cfg(d=64, E=E, I=64, Is=0, k=k, dtype="fp32", routed_scale=scale)
+    oidx, ow, margin = orc.select(c, logits.numpy(), bias.numpy())
+    gi, gw = got["idx"].cpu().numpy(), got["w"].cpu().numpy()
+    set_diff, order_bad = parity.selection_diff(gi, oidx, parity.biased_scores(logits.numpy(), bias.numpy()))
+    assert not (set_diff & (margin >= parity.NEAR_TIE)).any()
+    assert not order_bad.any()
+    ok = ~set_diff
+    np.testing.assert_allclose(parity.by_expert(gi[ok], gw[ok]), parity.by_expert(oidx[ok], ow[ok]),
+                               rtol=2e-6, atol=1e-7)
+
+
+def test_route_static_rejects_overlapping_buffers():
+    T, E, k = 300, 16, 2
+    logits = torch.zeros((T, E), dtype=torch.float32, device="cuda")
+    bias = torch.zeros(E, dtype=torch.float32, device="cuda")
+    # w written over the logits it reads
+    with pytest.raises(B.MoeError) as ei:
+        B.route_static(logits, bias, k, 1.0, out={"w": logits.view(-1)[: T * k]})
+    assert ei.value.status == B.MOE_ERR_INVALID_ARG
+    # two outputs sharing memory
+    buf = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    with pytest.raises(B.MoeError) as ei:
+        B.route_static(logits, bias, k, 1.0, out={"pos": buf.view(T, k), "row_tok": buf})
+    assert ei.value.status == B.MOE_ERR_INVALID_ARG
