@@ -66,7 +66,6 @@ struct PairCursor {
     int f0;      // first feature of this CTA's A rows
     int r0;      // first token row of this CTA's B half
     int nb;      // B bytes this CTA loads per k-block, in 8 KB units (one 64- or 128-row box)
-    int half;    // B rows of this CTA's half of the tile (MMA N / 2)
     bool valid;
     TileInfo ti;
 
@@ -74,7 +73,7 @@ struct PairCursor {
         valid = decode_tile(p, prefix, L, PR_BN, ti);
         if (!valid) return;
         const TcSeg& sg = p.seg[ti.seg];
-        half = ((ti.rows + 15) & ~15) >> 1;  // MMA N / 2, a multiple of 8
+        const int half = ((ti.rows + 15) & ~15) >> 1;  // MMA N / 2
         nb = half > 64 ? 2 : 1;
         f0 = ti.ftile * sg.a_fstride + static_cast<int>(rank) * sg.a_rank_off;
         r0 = ti.row0 + static_cast<int>(rank) * half;

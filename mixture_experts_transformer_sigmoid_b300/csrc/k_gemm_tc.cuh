@@ -74,8 +74,6 @@ struct TcSeg {
     int f_group;          // dense segment: feature tiles per tile group (0: all of them)
     int k_split;          // dense segment, single-CTA kernel: k-ranges per tile (0 or 1: none)
     int out_kind;         // weighted epilogue: OutKind of `out`
-    const int* b_rows;    // CTA-pair kernel: B row r of the tile is row b_rows[r] of map b (box one
-                          // row high, four rows per tile::gather4 copy); null: B rows are contiguous
 };
 
 struct TcParams {

@@ -259,19 +259,6 @@ __device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* m
         : "memory");
 }
 
-// Four rows of a 2-D tensor (row indices r0..r3, columns x .. x + box width)
-// into four consecutive box rows of this CTA's shared memory (the same
-// layout, swizzle included, as four rows of a tiled box load), counted on an
-// mbarrier of either CTA of the pair.  The tensor map's box is one row high.
-__device__ __forceinline__ void tma_gather4_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster, int x,
-                                                 int r0, int r1, int r2, int r3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.cta_group::2"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-        : "memory");
-}
-
 // Tensor memory of a CTA pair: one warp of each CTA takes part.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
