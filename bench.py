@@ -53,7 +53,15 @@ SWEEP_T = (1, 8, 16, 32, 128)   # decode token range (GLM-5 decode weights and b
 # stage, with the hash of the GEMM kernel sources it was taken on.  The bench
 # reports the figure only while the sources still hash to that value: any
 # change to the kernels makes it null until it is captured again.
-TRAFFIC_PER_LAUNCH = {}
+TRAFFIC_PER_LAUNCH = {
+    # glm5_slice (32 experts, 1024 tokens: the GLM-5 prefill's tokens per expert), one launch each
+    "glm5_slice": {"gate_up_swiglu": {"bytes": 1.903e9 + 0.036e9, "source_hash": "808ac0215b0334f5"},
+                   "down_weighted": {"bytes": 0.877e9 + 0.097e9, "source_hash": "808ac0215b0334f5"}},
+    # the same capture scaled by 8 to the GLM-5 prefill (routed experts and tokens grow 8x; the
+    # shared expert's weights do not, so this overstates by at most 7 x its 50 / 25 MB)
+    "glm5_prefill": {"gate_up_swiglu": {"bytes": 8 * (1.903e9 + 0.036e9), "source_hash": "808ac0215b0334f5"},
+                     "down_weighted": {"bytes": 8 * (0.877e9 + 0.097e9), "source_hash": "808ac0215b0334f5"}},
+}
 TRAFFIC_SOURCES = ("k_gemm_pair.cuh", "k_gemm_tc.cuh", "ptx.cuh")
 
 
@@ -98,6 +106,19 @@ def down_flops(w, T):
 
 def total_flops(w, T):
     return 2.0 * T * w.d * w.E + gate_up_flops(w, T) + down_flops(w, T)
+
+
+def gate_up_algorithmic_bytes(w, T):
+    """Bytes the gate|up launch must move at prefill sizes (every expert active):
+    the routed and shared weights, xn once, h and hs written (the permuted
+    copy xp is the implementation's, not the step's)."""
+    return 2 * (w.E * w.d * 2 * w.I + 2 * w.Is * w.d + T * w.d + T * w.k * w.I + T * w.Is)
+
+
+def down_algorithmic_bytes(w, T):
+    """The down launch: routed and shared weights, h and hs read, the fp16
+    weighted rows and the fp32 shared output written."""
+    return 2 * (w.E * w.I * w.d + w.d * w.Is + T * w.k * w.I + T * w.Is + T * w.k * w.d) + 4 * T * w.d
 
 
 def weight_bytes(w):
@@ -317,7 +338,11 @@ def run_ours(args, world, rank, local):
                 "peak_source": f"{peak_src} bf16 dense (burst)",
                 "flops_per_launch": dom_flops, "avg_launch_ms": round(dom_ms, 4),
                 "traffic": measured_traffic(w.name, dominant),
+                "algorithmic_bytes": (gate_up_algorithmic_bytes if dominant == "gate_up_swiglu"
+                                      else down_algorithmic_bytes)(w, T),
                 "kernel_source_hash": gemm_source_hash()}
+    if roofline["traffic"] is not None:
+        roofline["traffic_over_algorithmic"] = round(roofline["traffic"] / roofline["algorithmic_bytes"], 3)
     whole_tf = total_flops(w, T) / (ms / 1e3) / 1e12
     l2 = (f"inputs larger than L2 ({weight_bytes(w) / 1e9:.1f} GB of weights read every step)"
           if weight_bytes(w) > 126e6 else "inputs smaller than L2")

@@ -183,17 +183,20 @@ __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ ga
 // lane + 32, ... in order, then a shuffle reduction); the second pass reads
 // the row again (from L2: it was just read) and scales it.  Holding the row
 // in registers instead would take ~190 registers per thread for d = 6144 and
-// leave too few warps per SM to cover DRAM latency.
+// leave too few warps per SM to cover DRAM latency.  One warp per token:
+// a grid of one wave with each warp looping over tokens took 94 registers per
+// thread instead of 58 and measured slower.
 constexpr int RMS_WARP_U = 8;
 
 template <typename T>
-__global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const T* __restrict__ x, const T* __restrict__ gain,
-                                                           T* __restrict__ xn, int n_tok, int d, float eps) {
+__global__ void __launch_bounds__(256)
+    rmsnorm_warp_kernel(const T* __restrict__ x, const T* __restrict__ gain, T* __restrict__ xn, int n_tok, int d,
+                        float eps) {
     constexpr int V = Elem<T>::V;
     const int lane = threadIdx.x & 31;
-    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (t >= n_tok) return;
     const int nvec = d / V;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t < n_tok) {
     const int4* xr = reinterpret_cast<const int4*>(x + static_cast<size_t>(t) * d);
     float hi = 0.f, lo = 0.f;
     for (int v0 = 0; v0 < nvec; v0 += 32 * RMS_WARP_U) {
@@ -251,6 +254,7 @@ __global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const T* __restrict__
             store_vec<T>(xn + static_cast<size_t>(t) * d + v * V, f);
         }
     }
+    }
 }
 
 // RMSNorm fused with the router logits on CUDA cores (fp32 accumulation):
@@ -299,21 +303,23 @@ __global__ void rmsnorm_router_kernel(const T* __restrict__ x, const T* __restri
 
 // ------------------------------------------------------------------ top-k
 // Where the top-k kernel reads a token's logits from: the router's (hi, lo)
-// partial-sum pairs, rounded once here (and written to `logits` for
-// inspection), or plain fp32 logits given by the caller.
+// partial-sum pair, rounded once here (and recorded in `logits` for
+// inspection), or plain fp32 logits given by the caller.  load() only reads,
+// so that a lane's loads of all its experts are in flight together; record()
+// writes afterwards.
 struct LogitsFromPairs {
     const float2* __restrict__ part;
     float* __restrict__ logits;
     __device__ float load(size_t i) const {
         const float2 pv = part[i];
-        const float l = __fadd_rn(pv.x, pv.y);  // the (hi, lo) pair, rounded once
-        logits[i] = l;
-        return l;
+        return __fadd_rn(pv.x, pv.y);   // the (hi, lo) pair, rounded once
     }
+    __device__ void record(size_t i, float l) const { logits[i] = l; }
 };
 struct LogitsPlain {
     const float* __restrict__ logits;
     __device__ float load(size_t i) const { return logits[i]; }
+    __device__ void record(size_t, float) const {}
 };
 
 // One warp per token.  s = sigmoid(l), b = s + bias; k rounds of a warp
@@ -341,12 +347,18 @@ __global__ void topk_kernel(const Src src, const float* __restrict__ bias, int T
     for (int tl = warp; tl < sub_tokens; tl += nw) {
         const int t = first + tl;
         if (t >= T) break;
-        float bv[EPL], sv[EPL];
+        float bv[EPL], sv[EPL], lv[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            lv[i] = e < E ? src.load(static_cast<size_t>(t) * E + e) : 0.f;
+        }
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
             if (e < E) {
-                const float l = src.load(static_cast<size_t>(t) * E + e);
+                const float l = lv[i];
+                src.record(static_cast<size_t>(t) * E + e, l);
                 const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
                 const float b = __fadd_rn(s, bias[e]);
                 sv[i] = s;
@@ -548,14 +560,16 @@ __global__ void gather_rows_kernel(const T* __restrict__ xn, const int* __restri
 // out[t] = x[t] + sh[t] + sum_j yp[pos[t, j]] in fp32, slots in order, one
 // rounding at the end (yp rows already carry their routing weight).  On the
 // tensor-core path the shared expert's output sh is fp32 (ST) and the
-// weighted rows yp fp16 (YT); elsewhere both are the handle dtype.
+// weighted rows yp fp16 (YT); elsewhere both are the handle dtype.  Block
+// (t, y) covers token t's vectors y * blockDim.x + threadIdx.x, ... (small
+// batches split a row over several blocks so that its loads run in parallel).
 template <typename T, typename YT = T, typename ST = T>
 __global__ void combine_kernel(const T* __restrict__ x, const ST* __restrict__ sh,
                                const YT* __restrict__ yp, const int* __restrict__ pos, int d, int k,
                                T* __restrict__ out) {
     constexpr int V = Elem<T>::V;
     const size_t t = blockIdx.x;
-    for (int v = threadIdx.x; v < d / V; v += blockDim.x) {
+    for (int v = blockIdx.y * blockDim.x + threadIdx.x; v < d / V; v += gridDim.y * blockDim.x) {
         float acc[V], tmp[V];
         load_vec<T>(x + t * d + v * V, acc);
         if (sh != nullptr) {

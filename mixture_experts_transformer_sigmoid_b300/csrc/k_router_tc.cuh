@@ -227,17 +227,24 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
 // Adds the ksplit (hi, lo) partial pairs of each logit in range order with a
 // compensated fp32 sum and stores the result as the single pair (l, 0) of
 // range 0.  Each thread owns one (t, e) across all ranges, so it may
-// overwrite range 0 in place.
+// overwrite range 0 in place; eight ranges' loads are in flight at a time.
 __global__ void router_reduce_kernel(float2* __restrict__ part, int ksplit, size_t n) {
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
         float hi = 0.f, lo = 0.f;
-        for (int s = 0; s < ksplit; ++s) {
-            const float2 pv = part[static_cast<size_t>(s) * n + i];
-            float s2, e2;
-            two_sum_f(hi, pv.x, s2, e2);
-            hi = s2;
-            lo = __fadd_rn(lo, __fadd_rn(e2, pv.y));
+        for (int s0 = 0; s0 < ksplit; s0 += 8) {
+            float2 pv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (s0 + j < ksplit) pv[j] = part[static_cast<size_t>(s0 + j) * n + i];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (s0 + j >= ksplit) break;
+                float s2, e2;
+                two_sum_f(hi, pv[j].x, s2, e2);
+                hi = s2;
+                lo = __fadd_rn(lo, __fadd_rn(e2, pv[j].y));
+            }
         }
         part[i] = make_float2(__fadd_rn(hi, lo), 0.f);
     }

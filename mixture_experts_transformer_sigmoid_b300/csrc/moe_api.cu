@@ -363,6 +363,13 @@ int launch_router_tc(moe_handle* h, const void* router_w, const void* xn, int T,
     return cudaGetLastError() == cudaSuccess ? 2 : 0;
 }
 
+// Grid of the combine: a block per token, and for batches too small to fill
+// the SMs each row split over several blocks of 256 vectors.
+dim3 combine_grid(int Tn, int nvec, int num_sms) {
+    const int split = Tn >= 4 * num_sms ? 1 : std::max(1, (nvec + 255) / 256);
+    return dim3(Tn, split, 1);
+}
+
 struct FwdArgs {
     int T;
     const void *x, *norm_w, *router_w;
@@ -509,7 +516,8 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
         // I: combine with the residual
         mark(h, 8, st);
         if constexpr (std::is_same<T, __nv_bfloat16>::value)   // the tensor-core path stores bf16
-            combine_kernel<T, __half, float><<<Tn, 256, 0, st>>>(x, Is > 0 ? static_cast<const float*>(h->sh) : nullptr,
+            combine_kernel<T, __half, float><<<combine_grid(Tn, d / Elem<T>::V, h->num_sms), 256, 0, st>>>(
+                x, Is > 0 ? static_cast<const float*>(h->sh) : nullptr,
                                                                  static_cast<const __half*>(h->yp), h->pos, d, k,
                                                                  static_cast<T*>(a.out));
         h->launches += 1;
@@ -533,7 +541,8 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     }
     // I: combine with the residual
     mark(h, 8, st);
-    combine_kernel<T><<<Tn, 256, 0, st>>>(x, sh, yp, h->pos, d, k, static_cast<T*>(a.out));
+    combine_kernel<T><<<combine_grid(Tn, d / Elem<T>::V, h->num_sms), 256, 0, st>>>(x, sh, yp, h->pos, d, k,
+                                                                                  static_cast<T*>(a.out));
     h->launches += 1;
     mark(h, moe_handle::NSTAGE, st);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
