@@ -54,6 +54,9 @@ constexpr int DEVERR_RANGE = 2;     // an fp16 output overflowed (|v| > 65504)
 // RESIDUAL: out = res[row, col] + acc, added in fp32 and rounded once.
 // PARTIAL: fp32 acc of one k-range of a split dense segment, to
 //   out[k-range][row][col] (single-CTA kernel; the ranges are added later).
+//   With partial_halves set (a gate|up segment: A rows 64-127 are the up rows
+//   of the same features as rows 0-63), the second half goes to columns
+//   F + col, so a row of the partials holds all gates, then all ups.
 enum EpiKind { EPI_SWIGLU = 1, EPI_WEIGHTED = 2, EPI_RESIDUAL = 3, EPI_PARTIAL = 4 };
 enum OutKind { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2 };
 
@@ -74,6 +77,7 @@ struct TcSeg {
     int f_group;          // dense segment: feature tiles per tile group (0: all of them)
     int k_split;          // dense segment, single-CTA kernel: k-ranges per tile (0 or 1: none)
     int out_kind;         // weighted epilogue: OutKind of `out`
+    int partial_halves;   // partial epilogue: rows 64-127 of A are a second half (see EPI_PARTIAL)
 };
 
 struct TcParams {
@@ -416,7 +420,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         if (!(amax <= 65504.0f)) atomicOr(p.err, DEVERR_RANGE);
                     }
                 } else if constexpr (EPI == EPI_PARTIAL) {
-                    const int col = ti.ftile * sg.a_fstride + q * 32 + lane;
+                    const int fq = sg.partial_halves ? (q & 1) : q;
+                    const int col = ti.ftile * sg.a_fstride + fq * 32 + lane;
+                    const int coff = (sg.partial_halves && q >= 2) ? sg.F : 0;
                     float* part = static_cast<float*>(sg.out) +
                                   static_cast<size_t>(ti.ks) * sg.n_rows * sg.ld_out;
                     if (col < sg.F) {
@@ -424,7 +430,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
 #pragma unroll
                         for (int c = 0; c < 32; ++c) {
                             if (c >= cmax) break;
-                            part[static_cast<size_t>(ti.row0 + c0 + c) * sg.ld_out + col] = __uint_as_float(v[c]);
+                            part[static_cast<size_t>(ti.row0 + c0 + c) * sg.ld_out + coff + col] = __uint_as_float(v[c]);
                         }
                     }
                 } else if constexpr (EPI == EPI_RESIDUAL) {

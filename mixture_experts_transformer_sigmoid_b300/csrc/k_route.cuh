@@ -619,6 +619,36 @@ __global__ void splitk_residual_kernel(const float* __restrict__ part, int nspli
     }
 }
 
+// The dense block's split gate|up projection: h[t, f] = silu(g) * u with g
+// and u the sums, in k-range order, of the fp32 partials part[s][t][f] and
+// part[s][t][F + f], rounded once to the storage dtype (the same SwiGLU
+// arithmetic as the GEMM epilogue).  Four features per thread; F is a
+// multiple of 4.
+template <typename T>
+__global__ void splitk_swiglu_kernel(const float* __restrict__ part, int nsplit, int n_tok, int F,
+                                     T* __restrict__ h) {
+    const size_t stride = static_cast<size_t>(n_tok) * 2 * F;
+    const size_t n4 = static_cast<size_t>(n_tok) * F / 4;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t t = i / (F / 4), f = (i - t * (F / 4)) * 4;
+        const float* g0 = part + t * 2 * F + f;
+        float4 g = *reinterpret_cast<const float4*>(g0);
+        float4 u = *reinterpret_cast<const float4*>(g0 + F);
+        for (int sp = 1; sp < nsplit; ++sp) {
+            const float4 gs = *reinterpret_cast<const float4*>(g0 + sp * stride);
+            const float4 us = *reinterpret_cast<const float4*>(g0 + sp * stride + F);
+            g.x += gs.x; g.y += gs.y; g.z += gs.z; g.w += gs.w;
+            u.x += us.x; u.y += us.y; u.z += us.z; u.w += us.w;
+        }
+        T* o = h + t * F + f;
+        o[0] = Elem<T>::from_f(g.x / (1.0f + __expf(-g.x)) * u.x);
+        o[1] = Elem<T>::from_f(g.y / (1.0f + __expf(-g.y)) * u.y);
+        o[2] = Elem<T>::from_f(g.z / (1.0f + __expf(-g.z)) * u.z);
+        o[3] = Elem<T>::from_f(g.w / (1.0f + __expf(-g.w)) * u.w);
+    }
+}
+
 // The query compression's split-K epilogue, one block per token: c = the sum
 // of the k-range partials part[s][t] (s in order) rounded once to the
 // storage dtype (the Linear's output), then q = gain * cast(c * r) with r the

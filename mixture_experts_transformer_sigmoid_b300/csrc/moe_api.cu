@@ -62,6 +62,7 @@ struct moe_handle {
     void* sh = nullptr;
     void* hd = nullptr;       // dense block activations [max_tokens, dense_inter]
     float* dpart = nullptr;   // split-K partials of the dense down projection [DENSE_SPLIT_MAX][DENSE_SPLIT_MAX_T][d]
+    float* gpart = nullptr;   // split-K partials of the dense gate|up projection [DENSE_GU_SPLIT_MAX][DENSE_SPLIT_MAX_T][2 dense_inter]
     void* x_stage = nullptr;
     void* out_stage = nullptr;
     // pipelined host I/O (moe_forward_host_async): a second staging slot, copy
@@ -158,7 +159,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 void free_ws(moe_handle* h) {
     void* ptrs[] = {h->xn, h->logits, h->part, h->topk_idx, h->topk_w, h->chunk_cnt, h->chunk_base,
                     h->counts, h->offsets, h->pos, h->row_tok, h->row_w, h->xp, h->h, h->yp,
-                    h->hs, h->sh, h->hd, h->dpart, h->x_stage, h->out_stage, h->x_stage2,
+                    h->hs, h->sh, h->hd, h->dpart, h->gpart, h->x_stage, h->out_stage, h->x_stage2,
                     h->out_stage2, h->err};
     for (void* p : ptrs)
         if (p) cudaFree(p);
@@ -232,6 +233,25 @@ int dense_down_split(int Tn, int d, int Id, int num_sms) {
     if (Tn > DENSE_SPLIT_MAX_T) return 1;
     const int tiles = ((Tn + 63) / 64) * ((d + 127) / 128);
     return std::max(1, std::min({Id / 64, DENSE_SPLIT_MAX, num_sms / tiles}));
+}
+
+// Split-K of the dense gate|up projection for decode-sized batches: its
+// ceil(T / 64) * I / 64 tiles (192 at I = 12288) are 1.3 waves; k-ranges (at
+// most DENSE_GU_SPLIT_MAX) are chosen for the fullest last wave, and their
+// fp32 partials (gates, then ups) are added by splitk_swiglu_kernel.
+constexpr int DENSE_GU_SPLIT_MAX = 4;
+
+int dense_gate_up_split(int Tn, int d, int Id, int num_sms) {
+    if (Tn > DENSE_SPLIT_MAX_T) return 1;
+    const int tiles = ((Tn + 63) / 64) * (Id / 64);
+    int best = 1;
+    double best_eff = 0.0;
+    for (int ks = 1; ks <= std::min(DENSE_GU_SPLIT_MAX, d / 64); ++ks) {
+        const double waves = static_cast<double>(tiles) * ks / num_sms;
+        const double eff = waves / std::ceil(waves);   // busy fraction of the SMs over the launch
+        if (eff > best_eff + 0.02) { best_eff = eff; best = ks; }
+    }
+    return best;
 }
 
 void set_dense_groups(TcSeg& sg, int weight_rows_per_ftile) {
@@ -579,7 +599,22 @@ moe_status dense_impl(moe_handle* h, int Tn, const void* x_, const void* norm_w,
         g1.seg[0] = pair ? TcSeg{0, Tn, d, 128, 0, (Id + 127) / 128, Id, Id, hd, nullptr, 64, PA_TWO_2D, nullptr}
                          : TcSeg{0, Tn, d, 64, 0, Id / 64, Id, Id, hd, nullptr, 0, 0, nullptr};
         set_dense_groups(g1.seg[0], pair ? 256 : 128);
-        if (run_tc<EPI_SWIGLU>(g1, pair, Tn, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+        const int ks1 = (pair || h->gpart == nullptr) ? 1 : dense_gate_up_split(Tn, d, Id, h->num_sms);
+        if (ks1 > 1) {
+            // k-ranges of fp32 partials [ks1][Tn][gates | ups], then SwiGLU of their sums
+            g1.seg[0].out = h->gpart;
+            g1.seg[0].ld_out = 2 * Id;
+            g1.seg[0].k_split = ks1;
+            g1.seg[0].partial_halves = 1;
+            const int grid = std::max(1, std::min(h->num_sms, tile_bound(g1, 64, Tn)));
+            if (launch_tc<64, 8, EPI_PARTIAL>(g1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+            const size_t n4 = static_cast<size_t>(Tn) * Id / 4;
+            splitk_swiglu_kernel<T><<<static_cast<int>(std::min<size_t>((n4 + 255) / 256, 4 * h->num_sms)), 256, 0, st>>>(
+                h->gpart, ks1, Tn, Id, hd);
+            h->launches += 1;
+        } else if (run_tc<EPI_SWIGLU>(g1, pair, Tn, h->num_sms, st) != cudaSuccess) {
+            return MOE_ERR_CUDA;
+        }
         TcParams g2;
         std::memset(&g2, 0, sizeof g2);
         g2.E = 1;
@@ -947,7 +982,12 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out) {
     alloc(&h->yp, P * d * es);
     alloc(&h->hs, T * std::max<size_t>(Is, 1) * es);
     alloc(&h->sh, T * d * (tc ? 4 : es));   // the tensor-core path keeps the shared expert's output in fp32
-    if (c.dense_inter > 0) alloc(&h->hd, T * static_cast<size_t>(c.dense_inter) * es);
+    if (c.dense_inter > 0) {
+        alloc(&h->hd, T * static_cast<size_t>(c.dense_inter) * es);
+        if (tc)
+            alloc(&h->gpart, static_cast<size_t>(DENSE_GU_SPLIT_MAX) * std::min<size_t>(T, DENSE_SPLIT_MAX_T) * 2 *
+                                 static_cast<size_t>(c.dense_inter) * 4);
+    }
     // split-K partials of the dense down projection and of the query compression
     if (tc) alloc(&h->dpart, static_cast<size_t>(DENSE_SPLIT_MAX) * std::min<size_t>(T, DENSE_SPLIT_MAX_T) * d * 4);
     if (!dense_only) {   // host-I/O staging of moe_forward_host(_async)

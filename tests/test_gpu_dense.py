@@ -4,11 +4,10 @@ first first_k_dense_replace decoder layers use instead of the MoE (decoder
 layer excerpt on the GLM-5 shared-expert page).
 
 Small cases compare every token on both GEMM paths (single-CTA tiles below
-128 tokens, with the down projection split over k-ranges; CTA pairs from 128
+128 tokens, with both projections split over k-ranges; CTA pairs from 128
 up) and the CUDA-core path; the GLM-5-sized
 cases compare a seeded sample of tokens.  The output is held to the
-sublayer's tolerances (tests/parity.py, with its half-ulp allowance for the
-output's own rounding to bf16).  The MLP's own contribution
+sublayer's tolerances (tests/parity.py).  The MLP's own contribution
 out - x is checked too: in fp32 to 1e-4 of its rms; in bf16 elementwise to
 2^-8 |out| (the worst case of the one rounding of out to bf16, which is
 relative to |out|, not to the contribution) plus 2e-2 of its rms.  With the
