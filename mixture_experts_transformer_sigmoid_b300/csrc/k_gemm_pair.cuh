@@ -154,24 +154,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_pair_kernel(const __gri
         tmem_alloc_pair(tmem_holder, 2 * PR_BN);
         tmem_relinquish_pair();
     }
+    // barriers and tensor memory are set up before the wait for the previous
+    // kernel, which writes the offsets and every operand except the weights
+    grid_dep_wait();
     if (warp == 2) {
         bool any_grouped = false;
         for (int s = 0; s < p.n_segs; ++s) any_grouped |= (p.seg[s].grouped != 0);
         if (any_grouped) {
-            int run = 0;
-            for (int base = 0; base < p.E; base += 32) {
-                const int e = base + lane;
-                int v = 0;
-                if (e < p.E) v = (p.offsets[e + 1] - p.offsets[e] + PR_BN - 1) / PR_BN;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const int u = __shfl_up_sync(0xffffffffu, v, off);
-                    if (lane >= off) v += u;
-                }
-                if (e < p.E) prefix[e + 1] = run + v;
-                run += __shfl_sync(0xffffffffu, v, 31);
-            }
-            if (lane == 0) prefix[0] = 0;
+            tile_prefix(p.offsets, p.E, PR_BN, prefix, lane);
         }
     }
     tc_fence_before();

@@ -97,6 +97,37 @@ struct TileInfo {
     int ks, kb0, nkb;     // k-range of the tile: its index and k-blocks [kb0, kb0 + nkb)
 };
 
+// prefix[e] = token tiles (of BN rows) of the groups before e, for e = 0..E,
+// computed by one warp.  Each lane loads its groups' offsets for eight
+// 32-group blocks at once, so a launch pays about one round trip to memory
+// for E <= 256 instead of one per block.
+__device__ __forceinline__ void tile_prefix(const int* offsets, int E, int BN, int* prefix, int lane) {
+    constexpr int U = 8;
+    int run = 0;
+    for (int base = 0; base < E; base += 32 * U) {
+        int lo[U], hi[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = base + 32 * u + lane;
+            lo[u] = e < E ? offsets[e] : 0;
+            hi[u] = e < E ? offsets[e + 1] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = base + 32 * u + lane;
+            int v = (hi[u] - lo[u] + BN - 1) / BN;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int w = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += w;
+            }
+            if (e < E) prefix[e + 1] = run + v;
+            run += __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
+    if (lane == 0) prefix[0] = 0;
+}
+
 // Linear tile id -> (segment, group, first row, rows, feature tile).  Tiles
 // are ordered segment-major, then token tile, then feature tile, so CTAs that
 // run at the same time share the B tile and the L2 lines of the same expert.
@@ -221,25 +252,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         tmem_alloc(tmem_holder, 2 * BN);
         tmem_relinquish();
     }
+    // barriers and tensor memory are set up before the wait for the previous
+    // kernel, which writes the offsets and every operand except the weights
+    grid_dep_wait();
     if (warp == 2) {
         // prefix[e] = token tiles of groups < e (grouped segment)
         bool any_grouped = false;
         for (int s = 0; s < p.n_segs; ++s) any_grouped |= (p.seg[s].grouped != 0);
         if (any_grouped) {
-            int run = 0;
-            for (int base = 0; base < p.E; base += 32) {
-                const int e = base + lane;
-                int v = 0;
-                if (e < p.E) v = (p.offsets[e + 1] - p.offsets[e] + BN - 1) / BN;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const int u = __shfl_up_sync(0xffffffffu, v, off);
-                    if (lane >= off) v += u;
-                }
-                if (e < p.E) prefix[e + 1] = run + v;
-                run += __shfl_sync(0xffffffffu, v, 31);
-            }
-            if (lane == 0) prefix[0] = 0;
+            tile_prefix(p.offsets, p.E, BN, prefix, lane);
         }
     }
     tc_fence_before();

@@ -8,6 +8,7 @@
 #include <cstdint>
 
 #include "numeric.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -123,6 +124,7 @@ constexpr int RMS_REG_VECS = 4;
 template <typename T>
 __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ gain,
                                T* __restrict__ xn, int d, float eps) {
+    grid_dep_wait();
     __shared__ float2 red[33];
     constexpr int V = Elem<T>::V;
     const size_t t = blockIdx.x;
@@ -192,6 +194,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     rmsnorm_warp_kernel(const T* __restrict__ x, const T* __restrict__ gain, T* __restrict__ xn, int n_tok, int d,
                         float eps) {
+    grid_dep_wait();
     constexpr int V = Elem<T>::V;
     const int lane = threadIdx.x & 31;
     const int nvec = d / V;
@@ -322,6 +325,59 @@ struct LogitsPlain {
     __device__ void record(size_t, float) const {}
 };
 
+// The routing score of one logit: s = sigmoid(l) and the selection key
+// b = s + correction bias, a NaN key ranking last (keeps the order total).
+// Both top-k kernels call this, so they take the same decisions.
+__device__ __forceinline__ void router_score(float l, float bias_e, float& s, float& b) {
+    s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
+    const float bb = __fadd_rn(s, bias_e);
+    b = (bb == bb) ? bb : -INFINITY;
+}
+
+// Top-k of one token by one warp: k rounds of a warp argmax on (key bv
+// descending, expert index ascending) over the experts lane + 32 i held in
+// bv / sv (keys / sigmoid scores).  Slot j's expert and weight end up in lane
+// j: w_j = routed_scale * s_j / (s_0 + ... + s_{k-1}), the sum taken in slot
+// order.  Lanes j >= k get expert 0 and weight 0.
+template <int EPL>
+__device__ __forceinline__ void warp_select_topk(const float (&bv)[EPL], const float (&sv)[EPL], int E, int k,
+                                                 float routed_scale, int lane, int& my_e, float& my_w) {
+    my_e = 0;
+    float my_s = 0.f;
+    uint32_t removed = 0u;  // bit i: expert lane + 32 i already selected
+    for (int j = 0; j < k; ++j) {
+        // candidate of this lane: the best unselected expert it holds; every
+        // unselected expert is a candidate, so a winner always exists (k <= E)
+        float bb = 0.f, bs = 0.f;
+        int be = -1;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((removed >> i) & 1u) && (be < 0 || bv[i] > bb)) {
+                bb = bv[i];
+                be = e;
+                bs = sv[i];
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, bb, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            const float os = __shfl_xor_sync(0xffffffffu, bs, off);
+            if (oe >= 0 && (be < 0 || ob > bb || (ob == bb && oe < be))) {
+                bb = ob;
+                be = oe;
+                bs = os;
+            }
+        }
+        if ((be & 31) == lane) removed |= 1u << (be >> 5);
+        if (lane == j) { my_e = be; my_s = bs; }
+    }
+    float ssum = 0.f;
+    for (int j = 0; j < k; ++j) ssum = __fadd_rn(ssum, __shfl_sync(0xffffffffu, my_s, j));
+    my_w = lane < k ? __fdiv_rn(__fmul_rn(routed_scale, my_s), ssum) : 0.f;
+}
+
 // One warp per token.  s = sigmoid(l), b = s + bias; k rounds of a warp
 // argmax on (b descending, expert index ascending); slot j's expert and
 // sigmoid end up in lane j.  w_j = routed_scale * s_j / sum_i s_i.  Blocks
@@ -337,6 +393,7 @@ template <int EPL, typename Src>
 __global__ void topk_kernel(const Src src, const float* __restrict__ bias, int T, int E, int k,
                             float routed_scale, int* __restrict__ idx_out, float* __restrict__ w_out,
                             int* __restrict__ chunk_cnt, int split) {
+    grid_dep_wait();
     extern __shared__ int cnt[];  // [E]
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
@@ -359,52 +416,18 @@ __global__ void topk_kernel(const Src src, const float* __restrict__ bias, int T
             if (e < E) {
                 const float l = lv[i];
                 src.record(static_cast<size_t>(t) * E + e, l);
-                const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
-                const float b = __fadd_rn(s, bias[e]);
-                sv[i] = s;
-                bv[i] = (b == b) ? b : -INFINITY;  // a NaN score ranks last (keeps the order total)
+                router_score(l, bias[e], sv[i], bv[i]);
             } else {
                 sv[i] = 0.f;
                 bv[i] = 0.f;
             }
         }
-        int my_e = 0;
-        float my_s = 0.f;
-        uint32_t removed = 0u;  // bit i: expert lane + 32 i already selected
-        for (int j = 0; j < k; ++j) {
-            // candidate of this lane: the best unselected expert it holds; every
-            // unselected expert is a candidate, so a winner always exists (k <= E)
-            float bb = 0.f, bs = 0.f;
-            int be = -1;
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && !((removed >> i) & 1u) && (be < 0 || bv[i] > bb)) {
-                    bb = bv[i];
-                    be = e;
-                    bs = sv[i];
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ob = __shfl_xor_sync(0xffffffffu, bb, off);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-                if (oe >= 0 && (be < 0 || ob > bb || (ob == bb && oe < be))) {
-                    bb = ob;
-                    be = oe;
-                    bs = os;
-                }
-            }
-            if ((be & 31) == lane) removed |= 1u << (be >> 5);
-            if (lane == j) { my_e = be; my_s = bs; }
-        }
-        float ssum = 0.f;
-        for (int j = 0; j < k; ++j) ssum = __fadd_rn(ssum, __shfl_sync(0xffffffffu, my_s, j));
+        int my_e;
+        float my_w;
+        warp_select_topk<EPL>(bv, sv, E, k, routed_scale, lane, my_e, my_w);
         if (lane < k) {
             idx_out[static_cast<size_t>(t) * k + lane] = my_e;
-            w_out[static_cast<size_t>(t) * k + lane] =
-                __fdiv_rn(__fmul_rn(routed_scale, my_s), ssum);
+            w_out[static_cast<size_t>(t) * k + lane] = my_w;
             atomicAdd(&cnt[my_e], 1);
         }
     }
@@ -423,6 +446,7 @@ __global__ void topk_kernel(const Src src, const float* __restrict__ bias, int T
 __global__ void scan_kernel(const int* __restrict__ chunk_cnt, int n_chunks, int E,
                             int* __restrict__ counts, int* __restrict__ offsets,
                             int* __restrict__ chunk_base) {
+    grid_dep_wait();
     __shared__ int warp_tot[32];
     const int e = threadIdx.x;  // blockDim.x >= E, multiple of 32
     int total = 0;
@@ -468,6 +492,7 @@ __global__ void scatter_kernel(const int* __restrict__ idx, const float* __restr
                                int E, int k, const int* __restrict__ chunk_base,
                                int* __restrict__ pos, int* __restrict__ row_tok,
                                float* __restrict__ row_w) {
+    grid_dep_wait();
     extern __shared__ uint32_t mask[];  // [E][CHUNK_TOKENS / 32]
     constexpr int WORDS = CHUNK_TOKENS / 32;
     for (int i = threadIdx.x; i < E * WORDS; i += blockDim.x) mask[i] = 0u;
@@ -499,6 +524,7 @@ __global__ void scatter_kernel(const int* __restrict__ idx, const float* __restr
 template <typename T>
 __global__ void gather_tokens_kernel(const T* __restrict__ xn, const int* __restrict__ pos,
                                      T* __restrict__ xp, int n_tok, int k, int d, int P) {
+    grid_dep_wait();
     const int lane = threadIdx.x & 31;
     const int nvec = d * static_cast<int>(sizeof(T)) / 16;
     constexpr int U = 8;
@@ -536,6 +562,7 @@ __global__ void gather_tokens_kernel(const T* __restrict__ xn, const int* __rest
 template <typename T>
 __global__ void gather_rows_kernel(const T* __restrict__ xn, const int* __restrict__ row_tok,
                                    T* __restrict__ xp, int P, int d, int n_tok) {
+    grid_dep_wait();
     const int lane = threadIdx.x & 31;
     const int nvec = d * static_cast<int>(sizeof(T)) / 16;
     for (int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < P;
@@ -567,6 +594,7 @@ template <typename T, typename YT = T, typename ST = T>
 __global__ void combine_kernel(const T* __restrict__ x, const ST* __restrict__ sh,
                                const YT* __restrict__ yp, const int* __restrict__ pos, int d, int k,
                                T* __restrict__ out) {
+    grid_dep_wait();
     constexpr int V = Elem<T>::V;
     const size_t t = blockIdx.x;
     for (int v = blockIdx.y * blockDim.x + threadIdx.x; v < d / V; v += gridDim.y * blockDim.x) {
@@ -602,6 +630,7 @@ __global__ void combine_kernel(const T* __restrict__ x, const ST* __restrict__ s
 template <typename T>
 __global__ void splitk_residual_kernel(const float* __restrict__ part, int nsplit, size_t stride,
                                        const T* __restrict__ res, T* __restrict__ out, size_t n) {
+    grid_dep_wait();
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n / 4;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
         float4 acc = reinterpret_cast<const float4*>(part)[i];
@@ -627,6 +656,7 @@ __global__ void splitk_residual_kernel(const float* __restrict__ part, int nspli
 template <typename T>
 __global__ void splitk_swiglu_kernel(const float* __restrict__ part, int nsplit, int n_tok, int F,
                                      T* __restrict__ h) {
+    grid_dep_wait();
     const size_t stride = static_cast<size_t>(n_tok) * 2 * F;
     const size_t n4 = static_cast<size_t>(n_tok) * F / 4;
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
@@ -659,6 +689,7 @@ template <typename T>
 __global__ void splitk_rmsnorm_kernel(const float* __restrict__ part, int nsplit, size_t stride, int rank,
                                       const T* __restrict__ gain, float eps, T* __restrict__ c_out,
                                       T* __restrict__ q_out) {
+    grid_dep_wait();
     __shared__ float2 red[33];
     constexpr int V = Elem<T>::V;
     const size_t t = blockIdx.x;

@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
         tmem_alloc(tmem_holder, RT_NACC * 64);
         tmem_relinquish();
     }
+    grid_dep_wait();   // xn comes from the previous kernel
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -224,30 +225,37 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_tc_kernel(const __grid_c
     if (threadIdx.x == 0 && *abort_flag) atomicOr(p.err, 1);
 }
 
+// The compensated sum of logit i's ksplit (hi, lo) pairs, in range order,
+// as the single pair (l, 0); eight ranges' loads are in flight at a time.
+__device__ __forceinline__ float2 reduce_logit_pair(const float2* __restrict__ part, int ksplit, size_t n,
+                                                    size_t i) {
+    float hi = 0.f, lo = 0.f;
+    for (int s0 = 0; s0 < ksplit; s0 += 8) {
+        float2 pv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (s0 + j < ksplit) pv[j] = part[static_cast<size_t>(s0 + j) * n + i];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (s0 + j >= ksplit) break;
+            float s2, e2;
+            two_sum_f(hi, pv[j].x, s2, e2);
+            hi = s2;
+            lo = __fadd_rn(lo, __fadd_rn(e2, pv[j].y));
+        }
+    }
+    return make_float2(__fadd_rn(hi, lo), 0.f);
+}
+
 // Adds the ksplit (hi, lo) partial pairs of each logit in range order with a
 // compensated fp32 sum and stores the result as the single pair (l, 0) of
 // range 0.  Each thread owns one (t, e) across all ranges, so it may
-// overwrite range 0 in place; eight ranges' loads are in flight at a time.
+// overwrite range 0 in place.
 __global__ void router_reduce_kernel(float2* __restrict__ part, int ksplit, size_t n) {
+    grid_dep_wait();
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        float hi = 0.f, lo = 0.f;
-        for (int s0 = 0; s0 < ksplit; s0 += 8) {
-            float2 pv[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (s0 + j < ksplit) pv[j] = part[static_cast<size_t>(s0 + j) * n + i];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (s0 + j >= ksplit) break;
-                float s2, e2;
-                two_sum_f(hi, pv[j].x, s2, e2);
-                hi = s2;
-                lo = __fadd_rn(lo, __fadd_rn(e2, pv[j].y));
-            }
-        }
-        part[i] = make_float2(__fadd_rn(hi, lo), 0.f);
-    }
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        part[i] = reduce_logit_pair(part, ksplit, n, i);
 }
 
 }  // namespace moe

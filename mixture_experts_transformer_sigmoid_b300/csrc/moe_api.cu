@@ -31,9 +31,31 @@
 #include "k_pack.cuh"
 #include "k_route.cuh"
 #include "k_router_tc.cuh"
+#include "k_route_small.cuh"
 #include "moe.h"
 
 using namespace moe;
+
+// Launches a kernel on st with programmatic stream serialization: its blocks
+// may be scheduled once the kernel before it has exited, while that kernel's
+// memory operations are still being flushed.  Every kernel launched this way
+// calls grid_dep_wait before it touches global memory that an earlier kernel
+// writes or reads.  Errors are returned and also left for cudaGetLastError.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dep(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct moe_handle {
     moe_config cfg;
@@ -198,8 +220,7 @@ cudaError_t launch_tc(const TcParams& prm, int grid, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    tc_gemm_kernel<BN, STAGES, EPI><<<grid, TC_THREADS, S::TOTAL, st>>>(prm);
-    return cudaGetLastError();
+    return launch_dep(tc_gemm_kernel<BN, STAGES, EPI>, grid, TC_THREADS, S::TOTAL, st, prm);
 }
 
 // Upper bound of the tiles a launch can have (the exact count depends on
@@ -273,11 +294,13 @@ cudaError_t launch_pair(const TcParams& prm, int P, int num_sms, cudaStream_t st
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64) return cudaErrorInvalidDevice;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // as launch_dep
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(TC_THREADS, 1, 1);
     cfg.dynamicSmemBytes = PrSmem::TOTAL;
@@ -297,6 +320,7 @@ cudaError_t launch_pair(const TcParams& prm, int P, int num_sms, cudaStream_t st
     }
     const int clusters = std::max(1, std::min(max_clusters[dev], tile_bound(prm, PR_BN, P)));
     cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<EPI>, prm);
 }
 
@@ -329,8 +353,8 @@ void launch_topk_e(const Src& src, const float* bias, int T, int E, int k, float
     }
     const int nthreads = std::min(threads[dev], 32 * (CHUNK_TOKENS / split));
     if (split > 1) cudaMemsetAsync(chunk_cnt, 0, static_cast<size_t>(n_chunks) * E * sizeof(int), st);
-    topk_kernel<EPL, Src><<<n_chunks * split, nthreads, E * sizeof(int), st>>>(src, bias, T, E, k, scale, idx, w,
-                                                                               chunk_cnt, split);
+    launch_dep(topk_kernel<EPL, Src>, n_chunks * split, nthreads, E * sizeof(int), st,
+               src, bias, T, E, k, scale, idx, w, chunk_cnt, split);
 }
 
 template <typename Src>
@@ -348,8 +372,12 @@ void launch_topk(const Src& src, const float* bias, int T, int E, int k, float s
 
 // Router logits on the tensor cores.  Split-K is chosen so that small
 // batches still spread over the SMs; the ranges are then added by
-// router_reduce_kernel.  Returns the number of launches (0 on error).
-int launch_router_tc(moe_handle* h, const void* router_w, const void* xn, int T, cudaStream_t st) {
+// router_reduce_kernel, or, when defer is given and the partials are few
+// enough for one block to read, left to the fused small-batch routing kernel
+// (*defer = the number of ranges it must add; 1 when nothing is left).
+// Returns the number of launches (0 on error).
+int launch_router_tc(moe_handle* h, const void* router_w, const void* xn, int T, cudaStream_t st,
+                     int* defer = nullptr) {
     const int d = h->cfg.hidden, E = h->cfg.n_experts;
     RouterParams rp;
     std::memset(&rp, 0, sizeof rp);
@@ -375,12 +403,37 @@ int launch_router_tc(moe_handle* h, const void* router_w, const void* xn, int T,
             return 0;
         attr_set[dev] = true;
     }
-    router_tc_kernel<<<std::min(h->num_sms, tiles0 * ks), RT_THREADS, RT_SMEM, st>>>(rp);
+    launch_dep(router_tc_kernel, std::min(h->num_sms, tiles0 * ks), RT_THREADS, RT_SMEM, st, rp);
+    if (defer != nullptr) *defer = 1;
     if (ks == 1) return cudaGetLastError() == cudaSuccess ? 1 : 0;
     const size_t n = static_cast<size_t>(T) * E;
-    router_reduce_kernel<<<static_cast<int>(std::min<size_t>((n + 255) / 256, 4 * h->num_sms)), 256, 0,
-                           st>>>(h->part, ks, n);
+    if (defer != nullptr && n * ks <= static_cast<size_t>(RS_MAX_PAIRS)) {
+        *defer = ks;
+        return cudaGetLastError() == cudaSuccess ? 1 : 0;
+    }
+    launch_dep(router_reduce_kernel, static_cast<int>(std::min<size_t>((n + 255) / 256, 4 * h->num_sms)), 256, 0, st,
+               h->part, ks, n);
     return cudaGetLastError() == cudaSuccess ? 2 : 0;
+}
+
+// The fused small-batch routing block, instantiated for the experts per lane.
+template <int EPL>
+cudaError_t launch_route_small_e(const RouteSmallArgs& ra, cudaStream_t st) {
+    const size_t smem = route_small_smem(ra.T, ra.E, ra.k);
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(route_small_kernel<EPL>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    return launch_dep(route_small_kernel<EPL>, 1, RS_THREADS, smem, st, ra);
+}
+
+cudaError_t launch_route_small(const RouteSmallArgs& ra, cudaStream_t st) {
+    if (ra.E <= 32) return launch_route_small_e<1>(ra, st);
+    if (ra.E <= 64) return launch_route_small_e<2>(ra, st);
+    if (ra.E <= 128) return launch_route_small_e<4>(ra, st);
+    return launch_route_small_e<8>(ra, st);   // E <= RS_MAX_E = 256
 }
 
 // Grid of the combine: a block per token, and for batches too small to fill
@@ -408,6 +461,9 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     const int n_chunks = (Tn + CHUNK_TOKENS - 1) / CHUNK_TOKENS;
     const T* x = static_cast<const T*>(a.x);
     T* xn = static_cast<T*>(h->xn);
+    // decode-sized batches route in one block (route_small_kernel)
+    const bool small = h->tc && Tn <= RS_MAX_T && Tn * E <= RS_MAX_TE && E <= RS_MAX_E && k <= RS_MAX_K;
+    int ks_left = 1;
 
     // A+B: RMSNorm and router logits
     mark(h, 0, st);
@@ -415,12 +471,13 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
         // a warp per token once there are enough tokens to fill the SMs; small
         // batches (decode) keep a whole block on each token
         if (Tn >= 8 * h->num_sms)
-            rmsnorm_warp_kernel<T><<<(Tn + 7) / 8, 256, 0, st>>>(x, static_cast<const T*>(a.norm_w), xn, Tn,
-                                                                 d, c.eps);
+            launch_dep(rmsnorm_warp_kernel<T>, (Tn + 7) / 8, 256, 0, st,
+                       x, static_cast<const T*>(a.norm_w), xn, Tn, d, c.eps);
         else
-            rmsnorm_kernel<T><<<Tn, 256, 0, st>>>(x, static_cast<const T*>(a.norm_w), xn, d, c.eps);
+            launch_dep(rmsnorm_kernel<T>, Tn, 256, 0, st,
+                       x, static_cast<const T*>(a.norm_w), xn, d, c.eps);
         mark(h, 1, st);
-        const int n_router = launch_router_tc(h, a.router_w, xn, Tn, st);
+        const int n_router = launch_router_tc(h, a.router_w, xn, Tn, st, small ? &ks_left : nullptr);
         if (n_router == 0) return MOE_ERR_CUDA;
         h->launches += 1 + n_router;
     } else {
@@ -432,25 +489,60 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     }
     // C+D: top-k, weights, chunk histograms; E: scan, scatter, gather
     mark(h, 2, st);
-    launch_topk(LogitsFromPairs{h->part, h->logits}, a.bias, Tn, E, k, a.scale, h->topk_idx, h->topk_w,
-                h->chunk_cnt, h->num_sms, st);
-    mark(h, 3, st);
-    scan_kernel<<<1, std::max(32, (E + 31) / 32 * 32), 0, st>>>(h->chunk_cnt, n_chunks, E,
-                                                               h->counts, h->offsets, h->chunk_base);
-    mark(h, 4, st);
-    scatter_kernel<<<n_chunks, CHUNK_TOKENS, E * (CHUNK_TOKENS / 32) * sizeof(uint32_t), st>>>(
-        h->topk_idx, h->topk_w, Tn, E, k, h->chunk_base, h->pos, h->row_tok, h->row_w);
-    mark(h, 5, st);
+    bool gathered = false;
+    if (small) {
+        // one block from the logit partials to the permuted rows; the rows are
+        // gathered there too when they are few
+        RouteSmallArgs ra;
+        ra.part = h->part;
+        ra.ksplit = ks_left;
+        ra.bias = a.bias;
+        ra.logits = h->logits;
+        ra.T = Tn;
+        ra.E = E;
+        ra.k = k;
+        ra.routed_scale = a.scale;
+        ra.idx = h->topk_idx;
+        ra.w = h->topk_w;
+        ra.counts = h->counts;
+        ra.offsets = h->offsets;
+        ra.pos = h->pos;
+        ra.row_tok = h->row_tok;
+        ra.row_w = h->row_w;
+        ra.xn = xn;
+        gathered = static_cast<size_t>(P) * d * sizeof(T) <= RS_GATHER_MAX_BYTES;
+        ra.xp = gathered ? h->xp : nullptr;
+        ra.row_bytes = d * static_cast<int>(sizeof(T));
+        if (launch_route_small(ra, st) != cudaSuccess) return MOE_ERR_CUDA;
+        mark(h, 3, st);
+        mark(h, 4, st);
+        mark(h, 5, st);
+        h->launches += 1;
+    } else {
+        launch_topk(LogitsFromPairs{h->part, h->logits}, a.bias, Tn, E, k, a.scale, h->topk_idx, h->topk_w,
+                    h->chunk_cnt, h->num_sms, st);
+        mark(h, 3, st);
+        launch_dep(scan_kernel, 1, std::max(32, (E + 31) / 32 * 32), 0, st,
+                   h->chunk_cnt, n_chunks, E, h->counts, h->offsets, h->chunk_base);
+        mark(h, 4, st);
+        launch_dep(scatter_kernel, n_chunks, CHUNK_TOKENS, E * (CHUNK_TOKENS / 32) * sizeof(uint32_t), st,
+                   h->topk_idx, h->topk_w, Tn, E, k, h->chunk_base, h->pos, h->row_tok, h->row_w);
+        mark(h, 5, st);
+        h->launches += 3;
+    }
     // CTA pairs (256 x 256 tiles) once experts average 64 tokens or more; below
     // that the single-CTA kernel with 64-token tiles wastes less.
     const bool pair = h->tc && P >= 64 * E;
-    if (Tn >= 8 * h->num_sms)   // a warp per token: each xn row read once
-        gather_tokens_kernel<T><<<std::min(8 * h->num_sms, (Tn + 7) / 8), 256, 0, st>>>(
-            xn, h->pos, static_cast<T*>(h->xp), Tn, k, d, P);
-    else                        // few tokens: a warp per row spreads the copy over more SMs
-        gather_rows_kernel<T><<<std::min(4 * h->num_sms, (P + 7) / 8), 256, 0, st>>>(
-            xn, h->row_tok, static_cast<T*>(h->xp), P, d, Tn);
-    h->launches += 4;
+    if (gathered) {
+    } else if (Tn >= 8 * h->num_sms) {   // a warp per token: each xn row read once
+        launch_dep(gather_tokens_kernel<T>, std::min(8 * h->num_sms, (Tn + 7) / 8), 256, 0, st,
+                   xn, h->pos, static_cast<T*>(h->xp), Tn, k, d, P);
+        h->launches += 1;
+    } else {                            // few tokens: a warp per row spreads the copy over more SMs
+        launch_dep(gather_rows_kernel<T>, std::min(4 * h->num_sms, (P + 7) / 8), 256, 0, st,
+                   xn, h->row_tok, static_cast<T*>(h->xp), P, d, Tn);
+        h->launches += 1;
+    }
     mark(h, 6, st);
 
     T* hbuf = static_cast<T*>(h->h);
@@ -536,10 +628,9 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
         // I: combine with the residual
         mark(h, 8, st);
         if constexpr (std::is_same<T, __nv_bfloat16>::value)   // the tensor-core path stores bf16
-            combine_kernel<T, __half, float><<<combine_grid(Tn, d / Elem<T>::V, h->num_sms), 256, 0, st>>>(
-                x, Is > 0 ? static_cast<const float*>(h->sh) : nullptr,
-                                                                 static_cast<const __half*>(h->yp), h->pos, d, k,
-                                                                 static_cast<T*>(a.out));
+            launch_dep(combine_kernel<T, __half, float>, combine_grid(Tn, d / Elem<T>::V, h->num_sms), 256, 0, st,
+                       x, Is > 0 ? static_cast<const float*>(h->sh) : nullptr,
+                       static_cast<const __half*>(h->yp), h->pos, d, k, static_cast<T*>(a.out));
         h->launches += 1;
         mark(h, moe_handle::NSTAGE, st);
         return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -561,8 +652,8 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     }
     // I: combine with the residual
     mark(h, 8, st);
-    combine_kernel<T><<<combine_grid(Tn, d / Elem<T>::V, h->num_sms), 256, 0, st>>>(x, sh, yp, h->pos, d, k,
-                                                                                  static_cast<T*>(a.out));
+    launch_dep(combine_kernel<T>, combine_grid(Tn, d / Elem<T>::V, h->num_sms), 256, 0, st,
+               x, sh, yp, h->pos, d, k, static_cast<T*>(a.out));
     h->launches += 1;
     mark(h, moe_handle::NSTAGE, st);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -580,10 +671,11 @@ moe_status dense_impl(moe_handle* h, int Tn, const void* x_, const void* norm_w,
     T* xn = static_cast<T*>(h->xn);
     T* hd = static_cast<T*>(h->hd);
     if (Tn >= 8 * h->num_sms)
-        rmsnorm_warp_kernel<T><<<(Tn + 7) / 8, 256, 0, st>>>(x, static_cast<const T*>(norm_w), xn, Tn, d,
-                                                             c.eps);
+        launch_dep(rmsnorm_warp_kernel<T>, (Tn + 7) / 8, 256, 0, st,
+                   x, static_cast<const T*>(norm_w), xn, Tn, d, c.eps);
     else
-        rmsnorm_kernel<T><<<Tn, 256, 0, st>>>(x, static_cast<const T*>(norm_w), xn, d, c.eps);
+        launch_dep(rmsnorm_kernel<T>, Tn, 256, 0, st,
+                   x, static_cast<const T*>(norm_w), xn, d, c.eps);
     if (h->tc) {
         // CTA pairs (256 x 256 tiles) from two 64-token tiles up
         const bool pair = Tn >= 128;
@@ -609,8 +701,9 @@ moe_status dense_impl(moe_handle* h, int Tn, const void* x_, const void* norm_w,
             const int grid = std::max(1, std::min(h->num_sms, tile_bound(g1, 64, Tn)));
             if (launch_tc<64, 8, EPI_PARTIAL>(g1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
             const size_t n4 = static_cast<size_t>(Tn) * Id / 4;
-            splitk_swiglu_kernel<T><<<static_cast<int>(std::min<size_t>((n4 + 255) / 256, 4 * h->num_sms)), 256, 0, st>>>(
-                h->gpart, ks1, Tn, Id, hd);
+            launch_dep(splitk_swiglu_kernel<T>,
+                       static_cast<int>(std::min<size_t>((n4 + 255) / 256, 4 * h->num_sms)), 256, 0, st,
+                       h->gpart, ks1, Tn, Id, hd);
             h->launches += 1;
         } else if (run_tc<EPI_SWIGLU>(g1, pair, Tn, h->num_sms, st) != cudaSuccess) {
             return MOE_ERR_CUDA;
@@ -642,8 +735,9 @@ moe_status dense_impl(moe_handle* h, int Tn, const void* x_, const void* norm_w,
             const int grid = std::max(1, std::min(h->num_sms, tile_bound(g2, 64, Tn)));
             if (launch_tc<64, 8, EPI_PARTIAL>(g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
             const size_t n = static_cast<size_t>(Tn) * d;
-            splitk_residual_kernel<T><<<static_cast<int>(std::min<size_t>((n / 4 + 255) / 256, 4 * h->num_sms)), 256,
-                                        0, st>>>(h->dpart, ks, n, x, static_cast<T*>(out), n);
+            launch_dep(splitk_residual_kernel<T>,
+                       static_cast<int>(std::min<size_t>((n / 4 + 255) / 256, 4 * h->num_sms)), 256, 0, st,
+                       h->dpart, ks, n, x, static_cast<T*>(out), n);
             h->launches += 4;
         } else {
             if (run_tc<EPI_RESIDUAL>(g2, pair, Tn, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
@@ -673,11 +767,11 @@ moe_status q_latent_impl(moe_handle* h, int Tn, int rank, const void* hidden, co
     T* cq = static_cast<T*>(c_out);
     auto norm = [&]() {
         if (Tn >= 8 * h->num_sms)
-            rmsnorm_warp_kernel<T><<<(Tn + 7) / 8, 256, 0, st>>>(cq, static_cast<const T*>(gain),
-                                                                 static_cast<T*>(q_out), Tn, rank, c.eps);
+            launch_dep(rmsnorm_warp_kernel<T>, (Tn + 7) / 8, 256, 0, st,
+                       cq, static_cast<const T*>(gain), static_cast<T*>(q_out), Tn, rank, c.eps);
         else
-            rmsnorm_kernel<T><<<Tn, 256, 0, st>>>(cq, static_cast<const T*>(gain), static_cast<T*>(q_out),
-                                                  rank, c.eps);
+            launch_dep(rmsnorm_kernel<T>, Tn, 256, 0, st,
+                       cq, static_cast<const T*>(gain), static_cast<T*>(q_out), rank, c.eps);
     };
     if (!h->tc) {
         simt_shared_down_kernel<T><<<dim3(Tn, (rank + 127) / 128), 128, d * sizeof(float), st>>>(
@@ -720,9 +814,9 @@ moe_status q_latent_impl(moe_handle* h, int Tn, int rank, const void* hidden, co
         g.seg[0].k_split = ks;
         const int grid = std::max(1, std::min(grid_cap, tile_bound(g, 64, Tn)));
         if (launch_tc<64, 8, EPI_PARTIAL>(g, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
-        splitk_rmsnorm_kernel<T><<<Tn, 256, 0, st>>>(h->dpart, ks, static_cast<size_t>(Tn) * rank, rank,
-                                                     static_cast<const T*>(gain), c.eps, cq,
-                                                     static_cast<T*>(q_out));
+        launch_dep(splitk_rmsnorm_kernel<T>, Tn, 256, 0, st,
+                   h->dpart, ks, static_cast<size_t>(Tn) * rank, rank, static_cast<const T*>(gain), c.eps, cq,
+                   static_cast<T*>(q_out));
     } else {
         if (run_tc<EPI_WEIGHTED>(g, false, Tn, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
         norm();
@@ -850,10 +944,10 @@ moe_status moe_route_static(int32_t T, int32_t E, int32_t top_k, float routed_sc
     int n_sms = 148;
     if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
     launch_topk(LogitsPlain{logits}, corr_bias, T, E, top_k, routed_scale, idx, w, chunk_cnt, n_sms, st);
-    scan_kernel<<<1, std::max(32, (E + 31) / 32 * 32), 0, st>>>(chunk_cnt, nch, E, counts, offsets,
-                                                               chunk_base);
-    scatter_kernel<<<nch, CHUNK_TOKENS, E * (CHUNK_TOKENS / 32) * sizeof(uint32_t), st>>>(
-        idx, w, T, E, top_k, chunk_base, pos, row_tok, row_w);
+    launch_dep(scan_kernel, 1, std::max(32, (E + 31) / 32 * 32), 0, st,
+               chunk_cnt, nch, E, counts, offsets, chunk_base);
+    launch_dep(scatter_kernel, nch, CHUNK_TOKENS, E * (CHUNK_TOKENS / 32) * sizeof(uint32_t), st,
+               idx, w, T, E, top_k, chunk_base, pos, row_tok, row_w);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -18,6 +18,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialization may be scheduled
+// before the kernel ahead of it in the stream has finished (here: once that
+// grid's blocks have exited, before its memory operations are flushed).
+// grid_dep_wait blocks the calling thread until every grid this launch
+// depends on has completed and its memory operations are visible; for a
+// launch without that attribute it returns at once.  Every kernel of the
+// forward calls it before its first access to global memory that another
+// kernel writes or reads.  (Letting the next grid start earlier, from inside
+// the running one, measured slower for decode-sized batches.)
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
