@@ -55,12 +55,12 @@ SWEEP_T = (1, 8, 16, 32, 128)   # decode token range (GLM-5 decode weights and b
 # change to the kernels makes it null until it is captured again.
 TRAFFIC_PER_LAUNCH = {
     # glm5_slice (32 experts, 1024 tokens: the GLM-5 prefill's tokens per expert), one launch each
-    "glm5_slice": {"gate_up_swiglu": {"bytes": 1.903e9 + 0.036e9, "source_hash": "808ac0215b0334f5"},
-                   "down_weighted": {"bytes": 0.877e9 + 0.097e9, "source_hash": "808ac0215b0334f5"}},
+    "glm5_slice": {"gate_up_swiglu": {"bytes": 1.9027e9 + 0.0365e9, "source_hash": "846a0149fe785314"},
+                   "down_weighted": {"bytes": 0.8758e9 + 0.0968e9, "source_hash": "846a0149fe785314"}},
     # the same capture scaled by 8 to the GLM-5 prefill (routed experts and tokens grow 8x; the
     # shared expert's weights do not, so this overstates by at most 7 x its 50 / 25 MB)
-    "glm5_prefill": {"gate_up_swiglu": {"bytes": 8 * (1.903e9 + 0.036e9), "source_hash": "808ac0215b0334f5"},
-                     "down_weighted": {"bytes": 8 * (0.877e9 + 0.097e9), "source_hash": "808ac0215b0334f5"}},
+    "glm5_prefill": {"gate_up_swiglu": {"bytes": 8 * (1.9027e9 + 0.0365e9), "source_hash": "846a0149fe785314"},
+                     "down_weighted": {"bytes": 8 * (0.8758e9 + 0.0968e9), "source_hash": "846a0149fe785314"}},
 }
 TRAFFIC_SOURCES = ("k_gemm_pair.cuh", "k_gemm_tc.cuh", "ptx.cuh")
 
@@ -422,6 +422,50 @@ def run_ours(args, world, rank, local):
     return res
 
 
+def run_decode_only(args, T, local, peaks, peak_src, world):
+    """One decode batch of T tokens on the GLM-5 shapes (skewed routing), the
+    forward replayed from a CUDA graph with L2 flushed before every step: the
+    case for a launch list of a decode step."""
+    from mixture_experts_transformer_sigmoid_b300 import binding as B
+    w = wl.WORKLOADS["glm5_decode"]
+    inp = wl.make_inputs(w, seed=0, device="cuda", T=T)
+    layer = B.MoeSublayer(max_tokens=T, hidden=w.d, n_experts=w.E, inter=w.I, shared_inter=w.Is,
+                          max_top_k=w.k, dtype=w.dtype, eps=w.eps, device=local)
+    out = torch.empty_like(inp["x"])
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        layer.forward(inp["x"], inp, w.k, w.routed_scale, out=out)
+    assert layer.sync_status() == B.MOE_OK
+    _, _, counts = layer.routing()
+    n_active = int((counts > 0).sum().item())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(inp["x"], inp, w.k, w.routed_scale, out=out)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    assert layer.sync_status() == B.MOE_OK
+    ms = statistics.median([a.elapsed_time(b) for a, b in evs])
+    nbytes = decode_bytes(w, T, n_active)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    del graph
+    layer.close()
+    return {"metric": f"decode step ms (glm5_decode, {T} tokens)", "value": round(ms, 4), "unit": "ms",
+            "higher_is_better": False, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "n_active_experts": n_active, "bytes_per_step": nbytes, "hbm_gbs": round(gbs, 1),
+            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "dtype": "bf16",
+            "data": "synthetic (seeded, random-init weights)",
+            "l2": "256 MB buffer written between steps (outside the timed events)",
+            "launch": "CUDA graph replay of one moe_forward"}
+
+
 def run_decode(args, inp3, local, peaks, peak_src, world):
     from mixture_experts_transformer_sigmoid_b300 import binding as B
     w = wl.WORKLOADS["glm5_decode"]
@@ -723,6 +767,9 @@ def main():
     ap.add_argument("--only-dense", action="store_true",
                     help="time only the dense feed-forward block (about 1 GB on the device; "
                          "the case for profiling its kernels)")
+    ap.add_argument("--only-decode", type=int, default=0, metavar="T",
+                    help="time only a decode step of T tokens on the GLM-5 shapes (graph replay, "
+                         "L2 flushed; the case for a decode launch list)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--ref-budget-s", type=float, default=150.0,
                     help="reference arm: seconds of oracle work for the whole run")
@@ -736,6 +783,16 @@ def main():
             print(json.dumps(run_reference(args, world)), flush=True)
         return
     world, rank, local = dist_setup()
+    if args.only_decode > 0:
+        peaks, peak_src = load_peaks()
+        torch.cuda.set_device(local)
+        res = run_decode_only(args, args.only_decode, local, peaks, peak_src, world)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     if args.only_dense:
         peaks, peak_src = load_peaks()
         torch.cuda.set_device(local)

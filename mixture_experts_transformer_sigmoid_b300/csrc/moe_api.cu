@@ -376,15 +376,33 @@ void launch_topk(const Src& src, const float* bias, int T, int E, int k, float s
 // enough for one block to read, left to the fused small-batch routing kernel
 // (*defer = the number of ranges it must add; 1 when nothing is left).
 // Returns the number of launches (0 on error).
+// The router launch for a token tile width BN (see router_tc_kernel).
+template <int BN>
+cudaError_t launch_router_bn(const RouterParams& rp, int grid, cudaStream_t st) {
+    using C = RtCfg<BN>;
+    static bool attr_set[64] = {};   // per tile width and device, before the first launch
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(router_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    return launch_dep(router_tc_kernel<BN>, grid, C::THREADS, C::SMEM, st, rp);
+}
+
 int launch_router_tc(moe_handle* h, const void* router_w, const void* xn, int T, cudaStream_t st,
                      int* defer = nullptr) {
     const int d = h->cfg.hidden, E = h->cfg.n_experts;
+    const int BN = T > 64 ? 128 : 64;   // tokens per router tile
     RouterParams rp;
     std::memset(&rp, 0, sizeof rp);
-    if (!map_2d(&rp.a, router_w, d, E) || !map_2d(&rp.b, xn, d, T)) return 0;
+    if (!map_2d(&rp.a, router_w, d, E) || !map_2d(&rp.b, xn, d, T, BN)) return 0;
     const int nkb = d / 64;
-    const int tiles0 = ((T + RT_BN - 1) / RT_BN) * ((E + 127) / 128);
-    int ks = std::max(1, std::min((h->num_sms + tiles0 - 1) / tiles0, nkb / 4));
+    const int tiles0 = ((T + BN - 1) / BN) * ((E + 127) / 128);
+    int ks = std::max(1, std::min(h->num_sms / tiles0, nkb / 4));   // at most one wave
     const int kbps = (nkb + ks - 1) / ks;
     ks = (nkb + kbps - 1) / kbps;
     rp.T = T;
@@ -394,16 +412,9 @@ int launch_router_tc(moe_handle* h, const void* router_w, const void* xn, int T,
     rp.kb_per_split = kbps;
     rp.part = h->part;
     rp.err = h->err;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 0;
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 RT_SMEM) != cudaSuccess)
-            return 0;
-        attr_set[dev] = true;
-    }
-    launch_dep(router_tc_kernel, std::min(h->num_sms, tiles0 * ks), RT_THREADS, RT_SMEM, st, rp);
+    const int grid = std::min(h->num_sms, tiles0 * ks);
+    if ((BN == 128 ? launch_router_bn<128>(rp, grid, st) : launch_router_bn<64>(rp, grid, st)) != cudaSuccess)
+        return 0;
     if (defer != nullptr) *defer = 1;
     if (ks == 1) return cudaGetLastError() == cudaSuccess ? 1 : 0;
     const size_t n = static_cast<size_t>(T) * E;
@@ -1060,8 +1071,9 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out) {
     };
     alloc(&h->xn, T * d * es);
     alloc(&h->logits, T * E * 4);
-    // router partials: the split-K choice keeps ksplit * T below T + 64 * (number of SMs)
-    alloc(&h->part, (T + 64 * static_cast<size_t>(h->num_sms)) * E * sizeof(float2));
+    // router partials: the split-K choice (ksplit <= SMs / token tiles of BN <= RT_BN_MAX
+    // tokens) keeps ksplit * T below T + RT_BN_MAX * (number of SMs)
+    alloc(&h->part, (T + static_cast<size_t>(RT_BN_MAX) * h->num_sms) * E * sizeof(float2));
     alloc(&h->topk_idx, T * k * 4);
     alloc(&h->topk_w, T * k * 4);
     alloc(&h->chunk_cnt, nch * E * 4);
