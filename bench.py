@@ -55,12 +55,12 @@ SWEEP_T = (1, 8, 16, 32, 128)   # decode token range (GLM-5 decode weights and b
 # change to the kernels makes it null until it is captured again.
 TRAFFIC_PER_LAUNCH = {
     # glm5_slice (32 experts, 1024 tokens: the GLM-5 prefill's tokens per expert), one launch each
-    "glm5_slice": {"gate_up_swiglu": {"bytes": 1.9027e9 + 0.0365e9, "source_hash": "846a0149fe785314"},
-                   "down_weighted": {"bytes": 0.8758e9 + 0.0968e9, "source_hash": "846a0149fe785314"}},
+    "glm5_slice": {"gate_up_swiglu": {"bytes": 1.9038e9 + 0.0363e9, "source_hash": "d375e9479c2fa770"},
+                   "down_weighted": {"bytes": 0.8784e9 + 0.0972e9, "source_hash": "d375e9479c2fa770"}},
     # the same capture scaled by 8 to the GLM-5 prefill (routed experts and tokens grow 8x; the
     # shared expert's weights do not, so this overstates by at most 7 x its 50 / 25 MB)
-    "glm5_prefill": {"gate_up_swiglu": {"bytes": 8 * (1.9027e9 + 0.0365e9), "source_hash": "846a0149fe785314"},
-                     "down_weighted": {"bytes": 8 * (0.8758e9 + 0.0968e9), "source_hash": "846a0149fe785314"}},
+    "glm5_prefill": {"gate_up_swiglu": {"bytes": 8 * (1.9038e9 + 0.0363e9), "source_hash": "d375e9479c2fa770"},
+                     "down_weighted": {"bytes": 8 * (0.8784e9 + 0.0972e9), "source_hash": "d375e9479c2fa770"}},
 }
 TRAFFIC_SOURCES = ("k_gemm_pair.cuh", "k_gemm_tc.cuh", "ptx.cuh")
 
@@ -622,8 +622,9 @@ def run_dense(args, local, peaks, peak_src, world):
                 "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
                 "peak_source": f"{peak_src} HBM copy",
                 "l2": "256 MB buffer written between steps (outside the timed events)",
-                "launch": "CUDA graph replay of one moe_dense_forward (4 kernels: the down "
-                          "projection split over k-ranges, then their fixed-order sum)"}
+                "launch": "CUDA graph replay of one moe_dense_forward (5 kernels: RMSNorm, both "
+                          "projections split over k-ranges, each followed by the fixed-order sum of its "
+                          "partials)"}
         assert layer.sync_status() == B.MOE_OK
         del graph
     layer.close()
