@@ -86,6 +86,18 @@ def measured_traffic(workload: str, stage: str):
 GEMM_KERNEL = "tc_gemm_pair_kernel"
 
 
+# Every line after the headline prefill is timed after this much idle: the
+# power cap lowers the SM clock under the lines that run before it, so without
+# it a line's number would depend on which line ran before (a decode loop,
+# for one, never runs in the clock state a long prefill leaves behind).
+SETTLE_S = 0.5
+
+
+def settle():
+    torch.cuda.synchronize()
+    time.sleep(SETTLE_S)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -487,7 +499,7 @@ def run_decode(args, inp3, local, peaks, peak_src, world):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         layer.forward(dinp["x"], dinp, w.k, w.routed_scale, out=out)
-    torch.cuda.synchronize()
+    settle()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n_iter)]
     for a, b in evs:
@@ -551,6 +563,7 @@ def run_decode(args, inp3, local, peaks, peak_src, world):
             "tokens_per_s": round(world * w.T / (ms / 1e3), 1),
             "bytes_per_step": nbytes, "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
             "l2": "256 MB buffer written between steps (outside the timed events)",
+            "idle_before_s": SETTLE_S,
             "launch": "CUDA graph replay of one moe_forward",
             "roofline": {"kernel": "tc_gemm_kernel (gate_up_swiglu)", "bound": "hbm",
                          "achieved": round(gu_gbs, 1), "peak": hbm, "unit": "GB/s",
@@ -573,7 +586,8 @@ def run_dense(args, local, peaks, peak_src, world):
                           max_top_k=0, dtype=wp.dtype, eps=wp.eps, device=local, dense_inter=wp.I)
     stream = torch.cuda.current_stream()
     res = {}
-    for w, x in ((wp, inp["x"]), (wd, dinp["x"])):
+    # the decode-sized batch first, after the idle of settle(); then the prefill
+    for w, x in ((wd, dinp["x"]), (wp, inp["x"])):
         out = torch.empty_like(x)
         for _ in range(args.warmup):
             layer.dense_forward(x, inp, out=out)
@@ -587,6 +601,7 @@ def run_dense(args, local, peaks, peak_src, world):
             # weights (453 MB) and activations exceed L2: no flush between steps
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
+            settle()
             e0.record(stream)
             for _ in range(args.steps):
                 graph.replay()
@@ -600,13 +615,14 @@ def run_dense(args, local, peaks, peak_src, world):
                 "tokens_per_s": round(world * w.T / (ms / 1e3), 1), "flops_per_step": flops,
                 "tflops": round(tf, 1), "tensor_frac": round(tf / peaks["bf16_tflops"], 4),
                 "tensor_frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
-                "peak_source": f"{peak_src} bf16 dense (burst)",
+                "peak_source": f"{peak_src} bf16 dense (burst)", "idle_before_s": SETTLE_S,
                 "launch": "CUDA graph replay of one moe_dense_forward (3 kernels)"}
         else:
             flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
             n_iter = max(50, args.steps * 4)
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(n_iter)]
+            settle()
             for a, b in evs:
                 flush.zero_()
                 a.record(stream)
@@ -622,6 +638,7 @@ def run_dense(args, local, peaks, peak_src, world):
                 "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
                 "peak_source": f"{peak_src} HBM copy",
                 "l2": "256 MB buffer written between steps (outside the timed events)",
+                "idle_before_s": SETTLE_S,
                 "launch": "CUDA graph replay of one moe_dense_forward (5 kernels: RMSNorm, both "
                           "projections split over k-ranges, each followed by the fixed-order sum of its "
                           "partials)"}
@@ -657,6 +674,7 @@ def run_qlatent(args, local, peaks, peak_src, world):
         n_iter = max(50, args.steps * 4)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n_iter)]
+        settle()
         for a, b in evs:
             flush.zero_()                  # the weights (25 MB) would otherwise stay in L2
             a.record(stream)
@@ -676,7 +694,7 @@ def run_qlatent(args, local, peaks, peak_src, world):
                 "hbm_frac": round(nbytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                 "peak_source": f"{peak_src} (bf16 burst, HBM copy)",
                 "l2": "256 MB buffer written between steps (outside the timed events)",
-                "launch": "CUDA graph replay of one moe_q_latent"}
+                "launch": "CUDA graph replay of one moe_q_latent", "idle_before_s": SETTLE_S}
         res["prefill" if w.T >= 1024 else "decode"] = line
     layer.close()
     return res
@@ -704,6 +722,7 @@ def run_pack(args, inp, peaks, peak_src):
     n = max(3, min(args.steps, 10))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    settle()
     e0.record(stream)
     for _ in range(n):
         B.pack_experts(G, U, Dn, gate_up=gu, down_projs=dp)
@@ -716,7 +735,7 @@ def run_pack(args, inp, peaks, peak_src):
     torch.cuda.empty_cache()
     return {"experts": E, "hidden": d, "inter": I, "ms": round(ms, 4), "bytes": nbytes,
             "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
-            "peak_source": f"{peak_src} HBM copy", "exact": exact, "launches": 3,
+            "peak_source": f"{peak_src} HBM copy", "exact": exact, "launches": 3, "idle_before_s": SETTLE_S,
             "call": "moe_pack_experts (HF per-expert stacks -> gate_and_up_projs, down_projs)"}
 
 
