@@ -186,7 +186,8 @@ def test_glm5_workloads(name):
     workload_check(name, dev_gen=True)
 
 
-@pytest.mark.parametrize("name", ["ragged_bf16", "skewed_bf16"])   # CTA-pair / single-CTA GEMM paths
+# CTA-pair GEMMs / single-CTA GEMMs / single-CTA GEMMs with the fused decode routing
+@pytest.mark.parametrize("name", ["ragged_bf16", "skewed_bf16", "one_token_bf16"])
 def test_forward_replayed_from_cuda_graph_matches_direct_call(name):
     """moe_forward allocates nothing and never synchronises, so a serving loop
     can capture it in a CUDA graph; the replay must give the same bytes."""
