@@ -339,39 +339,52 @@ __device__ __forceinline__ void router_score(float l, float bias_e, float& s, fl
 // bv / sv (keys / sigmoid scores).  Slot j's expert and weight end up in lane
 // j: w_j = routed_scale * s_j / (s_0 + ... + s_{k-1}), the sum taken in slot
 // order.  Lanes j >= k get expert 0 and weight 0.
+// Each (key, expert) is packed into one 64-bit integer whose order is that
+// order: the key's bits mapped to an unsigned integer of the same order (after
+// -0 is made +0, so that the two tie as floats do) above the expert index
+// subtracted from 2^32 - 1.  A round's warp argmax is then a 64-bit max over
+// five shuffle levels, and one more shuffle fetches the winner's score from
+// the lane that holds it.  Keys are never NaN (router_score ranks NaN last as
+// -inf, whose mapped key is 0x007FFFFF); an expert already taken, or past E,
+// gets the key 0, below every real key.  Only the 32-bit keys are kept (the
+// 64-bit values would not fit the registers of a 1024-thread block).
 template <int EPL>
 __device__ __forceinline__ void warp_select_topk(const float (&bv)[EPL], const float (&sv)[EPL], int E, int k,
                                                  float routed_scale, int lane, int& my_e, float& my_w) {
+    uint32_t key[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        const uint32_t u = __float_as_uint(__fadd_rn(bv[i], 0.0f));
+        key[i] = e < E ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+    }
     my_e = 0;
     float my_s = 0.f;
-    uint32_t removed = 0u;  // bit i: expert lane + 32 i already selected
     for (int j = 0; j < k; ++j) {
-        // candidate of this lane: the best unselected expert it holds; every
-        // unselected expert is a candidate, so a winner always exists (k <= E)
-        float bb = 0.f, bs = 0.f;
-        int be = -1;
+        // candidate of this lane: the best expert it still holds (every
+        // unselected expert is a candidate, so a winner always exists: k <= E)
+        uint64_t cand = 0ull;
+        float cs = 0.f;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && !((removed >> i) & 1u) && (be < 0 || bv[i] > bb)) {
-                bb = bv[i];
-                be = e;
-                bs = sv[i];
-            }
+            const uint64_t v = (static_cast<uint64_t>(key[i]) << 32) |
+                               (0xFFFFFFFFu - static_cast<uint32_t>(lane + 32 * i));
+            if (v > cand) { cand = v; cs = sv[i]; }
         }
+        uint64_t win = cand;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-            const float ob = __shfl_xor_sync(0xffffffffu, bb, off);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-            if (oe >= 0 && (be < 0 || ob > bb || (ob == bb && oe < be))) {
-                bb = ob;
-                be = oe;
-                bs = os;
-            }
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, win, off);
+            win = o > win ? o : win;
         }
-        if ((be & 31) == lane) removed |= 1u << (be >> 5);
-        if (lane == j) { my_e = be; my_s = bs; }
+        const int we = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(win));
+        const float ws = __shfl_sync(0xffffffffu, cs, we & 31);
+        if ((we & 31) == lane) {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (i == (we >> 5)) key[i] = 0u;
+        }
+        if (lane == j) { my_e = we; my_s = ws; }
     }
     float ssum = 0.f;
     for (int j = 0; j < k; ++j) ssum = __fadd_rn(ssum, __shfl_sync(0xffffffffu, my_s, j));
