@@ -181,8 +181,9 @@ __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ ga
 
 // The same RMSNorm with one warp per token (no block barriers).  The first
 // pass streams the row in batches of RMS_WARP_U 16-byte vectors per lane and
-// accumulates the compensated sum of squares (each lane takes vectors lane,
-// lane + 32, ... in order, then a shuffle reduction); the second pass reads
+// accumulates the sum of squares (each vector's in fp32, the vectors' with a
+// compensated sum: each lane takes vectors lane, lane + 32, ... in order,
+// then a shuffle reduction); the second pass reads
 // the row again (from L2: it was just read) and scales it.  Holding the row
 // in registers instead would take ~190 registers per thread for d = 6144 and
 // leave too few warps per SM to cover DRAM latency.  One warp per token:
@@ -213,16 +214,21 @@ __global__ void __launch_bounds__(256)
         for (int j = 0; j < RMS_WARP_U; ++j) {
             if (v0 + lane + 32 * j >= nvec) continue;
             const T* e = reinterpret_cast<const T*>(&raw[j]);
+            // the vector's V squares by an FMA chain (at most V roundings, a
+            // relative error below V * 2^-24 of the vector's sum), then one
+            // compensated add: the per-element error-free products and sums
+            // cost ten instructions an element, and the kernel is one wave whose
+            // arithmetic does not overlap its loads
+            float c = 0.f;
 #pragma unroll
             for (int i = 0; i < V; ++i) {
                 const float f = Elem<T>::to_f(e[i]);
-                const float p = __fmul_rn(f, f);
-                const float pe = fmaf(f, f, -p);
-                float s, er;
-                two_sum_f(hi, p, s, er);
-                hi = s;
-                lo = __fadd_rn(lo, __fadd_rn(er, pe));
+                c = fmaf(f, f, c);
             }
+            float s, er;
+            two_sum_f(hi, c, s, er);
+            hi = s;
+            lo = __fadd_rn(lo, er);
         }
     }
 #pragma unroll
