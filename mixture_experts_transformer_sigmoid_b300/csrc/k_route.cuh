@@ -36,11 +36,14 @@ template <> struct Elem<__half> {   // the weighted expert rows of the tensor-co
 };
 
 template <typename T>
-__device__ __forceinline__ void load_vec(const T* p, float (&f)[Elem<T>::V]) {
-    int4 raw = *reinterpret_cast<const int4*>(p);
+__device__ __forceinline__ void unpack_vec(const int4& raw, float (&f)[Elem<T>::V]) {
     const T* e = reinterpret_cast<const T*>(&raw);
 #pragma unroll
     for (int i = 0; i < Elem<T>::V; ++i) f[i] = Elem<T>::to_f(e[i]);
+}
+template <typename T>
+__device__ __forceinline__ void load_vec(const T* p, float (&f)[Elem<T>::V]) {
+    unpack_vec<T>(*reinterpret_cast<const int4*>(p), f);
 }
 template <typename T>
 __device__ __forceinline__ void store_vec(T* p, const float (&f)[Elem<T>::V]) {
@@ -609,6 +612,9 @@ __global__ void gather_rows_kernel(const T* __restrict__ xn, const int* __restri
 // weighted rows yp fp16 (YT); elsewhere both are the handle dtype.  Block
 // (t, y) covers token t's vectors y * blockDim.x + threadIdx.x, ... (small
 // batches split a row over several blocks so that its loads run in parallel).
+// The slots' rows are loaded COMBINE_U at a time before they are added (with
+// k a run-time count, a load-add loop kept one row load in flight per thread).
+constexpr int COMBINE_U = 8;
 template <typename T, typename YT = T, typename ST = T>
 __global__ void combine_kernel(const T* __restrict__ x, const ST* __restrict__ sh,
                                const YT* __restrict__ yp, const int* __restrict__ pos, int d, int k,
@@ -633,11 +639,21 @@ __global__ void combine_kernel(const T* __restrict__ x, const ST* __restrict__ s
 #pragma unroll
             for (int i = 0; i < V; ++i) acc[i] += tmp[i];
         }
-        for (int j = 0; j < k; ++j) {
-            const size_t row = static_cast<size_t>(pos[t * k + j]);
-            load_vec<YT>(yp + row * d + v * V, tmp);
+        static_assert(Elem<YT>::V == V, "one 16-byte vector of yp per vector of out");
+        for (int j0 = 0; j0 < k; j0 += COMBINE_U) {
+            int4 raw[COMBINE_U];
 #pragma unroll
-            for (int i = 0; i < V; ++i) acc[i] += tmp[i];
+            for (int u = 0; u < COMBINE_U; ++u)
+                if (j0 + u < k)
+                    raw[u] = *reinterpret_cast<const int4*>(
+                        yp + static_cast<size_t>(pos[t * k + j0 + u]) * d + v * V);
+#pragma unroll
+            for (int u = 0; u < COMBINE_U; ++u) {
+                if (j0 + u >= k) break;
+                unpack_vec<YT>(raw[u], tmp);
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[i] += tmp[i];
+            }
         }
         store_vec<T>(out + t * d + v * V, acc);
     }
