@@ -145,11 +145,17 @@ __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ ga
         }
         return;
     }
+    // the gain's vectors are loaded with the row's, so that the scaling after
+    // the reduction waits for no second round trip to memory
     float f[RMS_REG_VECS][V];
+    int4 graw[RMS_REG_VECS];
 #pragma unroll
     for (int j = 0; j < RMS_REG_VECS; ++j) {
         const int v = threadIdx.x + j * blockDim.x;
-        if (v < nvec) load_vec<T>(xr + v * V, f[j]);
+        if (v < nvec) {
+            load_vec<T>(xr + v * V, f[j]);
+            graw[j] = *reinterpret_cast<const int4*>(gain + v * V);
+        }
     }
     // the same compensated sum of squares as row_rrms, over the registers
     float hi = 0.f, lo = 0.f;
@@ -175,7 +181,7 @@ __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ ga
         const int v = threadIdx.x + j * blockDim.x;
         if (v >= nvec) continue;
         float g[V];
-        load_vec<T>(gain + v * V, g);
+        unpack_vec<T>(graw[j], g);
 #pragma unroll
         for (int i = 0; i < V; ++i) f[j][i] = __fmul_rn(g[i], Elem<T>::round_io(__fmul_rn(f[j][i], r)));
         store_vec<T>(xn + t * d + v * V, f[j]);
