@@ -430,13 +430,22 @@ int launch_router_tc(moe_handle* h, const void* router_w, const void* xn, int T,
 // The fused small-batch routing block, instantiated for the experts per lane.
 template <int EPL>
 cudaError_t launch_route_small_e(const RouteSmallArgs& ra, cudaStream_t st) {
-    const size_t smem = route_small_smem(ra.T, ra.E, ra.k);
-    if (smem > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(route_small_kernel<EPL>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(smem));
+    // the largest shared memory any batch it takes can need, set once per device
+    constexpr size_t SMEM_MAX = route_small_smem(RS_MAX_T, RS_MAX_TE / RS_MAX_T, RS_MAX_K) +
+                                sizeof(float) * 2 * RS_MAX_E;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(route_small_kernel<EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(SMEM_MAX));
         if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
     }
+    const size_t smem = route_small_smem(ra.T, ra.E, ra.k);
+    if (smem > SMEM_MAX) return cudaErrorInvalidValue;
     return launch_dep(route_small_kernel<EPL>, 1, RS_THREADS, smem, st, ra);
 }
 
