@@ -240,7 +240,10 @@ typedef struct {
                                         CUDA-core path), 1 router logits, 2 top-k, 3 scan,
                                         4 scatter, 5 row gather, 6 gate|up + SwiGLU (routed and
                                         shared), 7 down + routing weight (routed and shared),
-                                        8 combine + residual. */
+                                        8 combine + residual.  Batches of at most 32 tokens
+                                        (and 256 experts) on the tensor-core path route in one
+                                        kernel, counted in stage 2; stages 3 and 4 are then
+                                        empty, and so is 5 when that kernel gathered the rows. */
 } moe_stats;
 
 /* Turns per-stage CUDA-event timing on (enable != 0) or off.  Recording
