@@ -553,14 +553,13 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     // CTA pairs (256 x 256 tiles) once experts average 64 tokens or more; below
     // that the single-CTA kernel with 64-token tiles wastes less.
     const bool pair = h->tc && P >= 64 * E;
-    if (gathered) {
-    } else if (Tn >= 8 * h->num_sms) {   // a warp per token: each xn row read once
-        launch_dep(gather_tokens_kernel<T>, std::min(8 * h->num_sms, (Tn + 7) / 8), 256, 0, st,
-                   xn, h->pos, static_cast<T*>(h->xp), Tn, k, d, P);
-        h->launches += 1;
-    } else {                            // few tokens: a warp per row spreads the copy over more SMs
-        launch_dep(gather_rows_kernel<T>, std::min(4 * h->num_sms, (P + 7) / 8), 256, 0, st,
-                   xn, h->row_tok, static_cast<T*>(h->xp), P, d, Tn);
+    if (!gathered) {
+        if (Tn >= 8 * h->num_sms)   // a warp per token: each xn row read once
+            launch_dep(gather_tokens_kernel<T>, std::min(8 * h->num_sms, (Tn + 7) / 8), 256, 0, st,
+                       xn, h->pos, static_cast<T*>(h->xp), Tn, k, d, P);
+        else                        // few tokens: a warp per row spreads the copy over more SMs
+            launch_dep(gather_rows_kernel<T>, std::min(4 * h->num_sms, (P + 7) / 8), 256, 0, st,
+                       xn, h->row_tok, static_cast<T*>(h->xp), P, d, Tn);
         h->launches += 1;
     }
     mark(h, 6, st);
