@@ -114,8 +114,7 @@ __device__ __forceinline__ float row_rrms(const T* xr, int d, float eps, float2*
         }
     }
     block_sum_pair(hi, lo, red);
-    const float ms = static_cast<float>((static_cast<double>(hi) + static_cast<double>(lo)) /
-                                        static_cast<double>(d));
+    const float ms = mean_of_pair(hi, lo, d);
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
 }
 
@@ -173,8 +172,7 @@ __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ ga
         }
     }
     block_sum_pair(hi, lo, red);
-    const float ms = static_cast<float>((static_cast<double>(hi) + static_cast<double>(lo)) /
-                                        static_cast<double>(d));
+    const float ms = mean_of_pair(hi, lo, d);
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
 #pragma unroll
     for (int j = 0; j < RMS_REG_VECS; ++j) {
@@ -188,90 +186,178 @@ __global__ void rmsnorm_kernel(const T* __restrict__ x, const T* __restrict__ ga
     }
 }
 
-// The same RMSNorm with one warp per token (no block barriers).  The first
-// pass streams the row in batches of RMS_WARP_U 16-byte vectors per lane and
-// accumulates the sum of squares (each vector's in fp32, the vectors' with a
-// compensated sum: each lane takes vectors lane, lane + 32, ... in order,
-// then a shuffle reduction); the second pass reads
-// the row again (from L2: it was just read) and scales it.  Holding the row
-// in registers instead would take ~190 registers per thread for d = 6144 and
-// leave too few warps per SM to cover DRAM latency.  One warp per token:
-// a grid of one wave with each warp looping over tokens took 94 registers per
-// thread instead of 58 and measured slower.
-constexpr int RMS_WARP_U = 8;
+// One 16-byte vector of the RMSNorm output: gain * cast(x * r), each
+// product rounded as the storage dtype's is.  For bf16 the gain product is
+// one packed bf16 multiply: the product of two bf16 values is exact in fp32,
+// so rounding it once to bf16 gives what the fp32 multiply and the store's
+// rounding give.
+template <typename T>
+__device__ __forceinline__ int4 rms_scale_vec(const int4& raw, const int4& graw, float r) {
+    constexpr int V = Elem<T>::V;
+    float f[V], g[V];
+    unpack_vec<T>(raw, f);
+    unpack_vec<T>(graw, g);
+#pragma unroll
+    for (int i = 0; i < V; ++i) f[i] = __fmul_rn(g[i], Elem<T>::round_io(__fmul_rn(f[i], r)));
+    int4 out;
+    store_vec<T>(reinterpret_cast<T*>(&out), f);
+    return out;
+}
+template <>
+__device__ __forceinline__ int4 rms_scale_vec<__nv_bfloat16>(const int4& raw, const int4& graw, float r) {
+    const __nv_bfloat162* xv = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    const __nv_bfloat162* gv = reinterpret_cast<const __nv_bfloat162*>(&graw);
+    int4 out;
+    __nv_bfloat162* ov = reinterpret_cast<__nv_bfloat162*>(&out);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 xf = __bfloat1622float2(xv[i]);
+        ov[i] = __hmul2(gv[i], __floats2bfloat162_rn(__fmul_rn(xf.x, r), __fmul_rn(xf.y, r)));
+    }
+    return out;
+}
+
+// The same RMSNorm with a warp per token and the rows staged in shared
+// memory.  Each warp owns RMSB_NBUF row buffers, filled by untiled bulk
+// copies (cp.async.bulk) that complete on one mbarrier per buffer; a buffer
+// is refilled with the warp's next row as soon as its row is scaled.  The
+// scaling pass reads the row from shared memory instead of again from L2,
+// and the block holds the gain row in shared memory too.  With 12 KB rows,
+// sixteen warps of one buffer (39.8 us for 8192 x 6144 bf16) measured faster
+// than eight warps of two (43.0 us): the kernel is bound by the issue of its
+// dependent arithmetic more than by the copies' latency, and more warps hide
+// more of it (eight vectors in flight per lane instead of four did not).
+// The warps loop over tokens (stride: all warps of the grid).  Per lane the
+// arithmetic is that of a warp reading the row itself: vectors lane,
+// lane + 32, ... in order
+// (four at a time, for independent instructions), each vector's V squares
+// by an FMA chain (at most V roundings, a relative error below V * 2^-24 of
+// the vector's sum), the vectors added with a compensated sum, then a shuffle
+// reduction.  The waits are bounded: a copy that has not landed after
+// RMS_WAIT_NS sets the timeout bit of the device error flag, and the warp
+// waits (again bounded) for its copies in flight before it returns.
+// Shared memory: RMSB_NBUF barriers per warp (RMSB_WARPS_MAX slots), the
+// gain row, then RMSB_NBUF row buffers per warp.  Rows 16-byte aligned (d *
+// sizeof(T) a multiple of 16).
+constexpr int RMSB_WARPS_MAX = 16;
+constexpr int RMSB_NBUF = 1;
+constexpr int RMSB_U = 4;                          // vectors per lane in flight
+constexpr size_t RMSB_BAR_BYTES = (8 * RMSB_NBUF * RMSB_WARPS_MAX + 15) / 16 * 16;
+constexpr uint64_t RMS_WAIT_NS = 2000000000ull;   // 2 s
+constexpr uint64_t RMS_DRAIN_NS = 100000000ull;   // 100 ms
+
+__host__ __device__ constexpr size_t rmsb_smem(int warps, size_t row_bytes) {
+    return RMSB_BAR_BYTES + static_cast<size_t>(1 + RMSB_NBUF * warps) * row_bytes;
+}
+
+// Untiled bulk copy of `bytes` from global to shared memory, completing on
+// `bar` as that many transaction bytes (16-byte aligned addresses, bytes a
+// multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
 
 template <typename T>
-__global__ void __launch_bounds__(256)
-    rmsnorm_warp_kernel(const T* __restrict__ x, const T* __restrict__ gain, T* __restrict__ xn, int n_tok, int d,
-                        float eps) {
-    grid_dep_wait();
+__global__ void __launch_bounds__(32 * RMSB_WARPS_MAX)
+    rmsnorm_bulk_kernel(const T* __restrict__ x, const T* __restrict__ gain, T* __restrict__ xn, int n_tok, int d,
+                        float eps, int* __restrict__ err) {
+    extern __shared__ __align__(16) uint8_t rms_smem[];
     constexpr int V = Elem<T>::V;
-    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int stride = gridDim.x * (blockDim.x >> 5);
+    const uint32_t row_bytes = static_cast<uint32_t>(d) * sizeof(T);
     const int nvec = d / V;
-    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (t < n_tok) {
-    const int4* xr = reinterpret_cast<const int4*>(x + static_cast<size_t>(t) * d);
-    float hi = 0.f, lo = 0.f;
-    for (int v0 = 0; v0 < nvec; v0 += 32 * RMS_WARP_U) {
-        int4 raw[RMS_WARP_U];
-#pragma unroll
-        for (int j = 0; j < RMS_WARP_U; ++j) {
-            const int v = v0 + lane + 32 * j;
-            if (v < nvec) raw[j] = __ldg(xr + v);
-        }
-#pragma unroll
-        for (int j = 0; j < RMS_WARP_U; ++j) {
-            if (v0 + lane + 32 * j >= nvec) continue;
-            const T* e = reinterpret_cast<const T*>(&raw[j]);
-            // the vector's V squares by an FMA chain (at most V roundings, a
-            // relative error below V * 2^-24 of the vector's sum), then one
-            // compensated add: the per-element error-free products and sums
-            // cost ten instructions an element, and the kernel is one wave whose
-            // arithmetic does not overlap its loads
-            float c = 0.f;
-#pragma unroll
-            for (int i = 0; i < V; ++i) {
-                const float f = Elem<T>::to_f(e[i]);
-                c = fmaf(f, f, c);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(rms_smem) + RMSB_NBUF * warp;
+    int4* gs = reinterpret_cast<int4*>(rms_smem + RMSB_BAR_BYTES);
+    uint8_t* buf = rms_smem + RMSB_BAR_BYTES + static_cast<size_t>(1 + RMSB_NBUF * warp) * row_bytes;
+    int t = blockIdx.x * (blockDim.x >> 5) + warp;
+    // the gain is a weight (no kernel before this one writes it)
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) gs[v] = reinterpret_cast<const int4*>(gain)[v];
+    if (lane == 0) {
+        for (int b = 0; b < RMSB_NBUF; ++b) mbar_init(&bar[b], 1);
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    grid_dep_wait();
+    if (lane == 0) {
+        for (int b = 0; b < RMSB_NBUF; ++b) {
+            const int tb = t + b * stride;
+            if (tb < n_tok) {
+                mbar_arrive_expect_tx(&bar[b], row_bytes);
+                bulk_load(buf + b * row_bytes, x + static_cast<size_t>(tb) * d, row_bytes, &bar[b]);
             }
+        }
+    }
+    int j = 0;
+    for (; t < n_tok; ++j, t += stride) {
+        const int b = j % RMSB_NBUF;
+        const int4* row = reinterpret_cast<const int4*>(buf + b * row_bytes);
+        // every lane observes the phase, which makes the copied bytes visible to it
+        const bool landed = mbar_wait(&bar[b], (j / RMSB_NBUF) & 1, nullptr, RMS_WAIT_NS);
+        if (!__all_sync(0xffffffffu, landed)) break;
+        float hi = 0.f, lo = 0.f;
+        for (int v0 = lane; v0 < nvec; v0 += 32 * RMSB_U) {
+            float c[RMSB_U];
+#pragma unroll
+            for (int u = 0; u < RMSB_U; ++u) {
+                c[u] = 0.f;
+                const int v = v0 + 32 * u;
+                if (v < nvec) {
+                    const int4 raw = row[v];
+                    const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+                    for (int i = 0; i < V; ++i) {
+                        const float f = Elem<T>::to_f(e[i]);
+                        c[u] = fmaf(f, f, c[u]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < RMSB_U; ++u) {
+                if (v0 + 32 * u >= nvec) break;
+                float s, er;
+                two_sum_f(hi, c[u], s, er);
+                hi = s;
+                lo = __fadd_rn(lo, er);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float oh = __shfl_xor_sync(0xffffffffu, hi, off);
+            const float ol = __shfl_xor_sync(0xffffffffu, lo, off);
             float s, er;
-            two_sum_f(hi, c, s, er);
+            two_sum_f(hi, oh, s, er);
             hi = s;
-            lo = __fadd_rn(lo, er);
+            lo = __fadd_rn(__fadd_rn(lo, ol), er);
+        }
+        const float ms = mean_of_pair(hi, lo, d);
+        const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+        int4* out = reinterpret_cast<int4*>(xn + static_cast<size_t>(t) * d);
+        for (int v0 = lane; v0 < nvec; v0 += 32 * RMSB_U) {
+#pragma unroll
+            for (int u = 0; u < RMSB_U; ++u) {
+                const int v = v0 + 32 * u;
+                if (v < nvec) out[v] = rms_scale_vec<T>(row[v], gs[v], r);
+            }
+        }
+        // the buffer is refilled by the async proxy after every lane's reads
+        __syncwarp();
+        const int tn = t + RMSB_NBUF * stride;
+        if (lane == 0 && tn < n_tok) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive_expect_tx(&bar[b], row_bytes);
+            bulk_load(buf + b * row_bytes, x + static_cast<size_t>(tn) * d, row_bytes, &bar[b]);
         }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float oh = __shfl_xor_sync(0xffffffffu, hi, off);
-        const float ol = __shfl_xor_sync(0xffffffffu, lo, off);
-        float s, er;
-        two_sum_f(hi, oh, s, er);
-        hi = s;
-        lo = __fadd_rn(__fadd_rn(lo, ol), er);
-    }
-    const float ms = static_cast<float>((static_cast<double>(hi) + static_cast<double>(lo)) /
-                                        static_cast<double>(d));
-    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
-    for (int v0 = 0; v0 < nvec; v0 += 32 * RMS_WARP_U) {
-        int4 raw[RMS_WARP_U];
-#pragma unroll
-        for (int j = 0; j < RMS_WARP_U; ++j) {
-            const int v = v0 + lane + 32 * j;
-            if (v < nvec) raw[j] = __ldg(xr + v);
-        }
-#pragma unroll
-        for (int j = 0; j < RMS_WARP_U; ++j) {
-            const int v = v0 + lane + 32 * j;
-            if (v >= nvec) continue;
-            const T* e = reinterpret_cast<const T*>(&raw[j]);
-            float f[V], g[V];
-            load_vec<T>(gain + v * V, g);
-#pragma unroll
-            for (int i = 0; i < V; ++i)
-                f[i] = __fmul_rn(g[i], Elem<T>::round_io(__fmul_rn(Elem<T>::to_f(e[i]), r)));
-            store_vec<T>(xn + static_cast<size_t>(t) * d + v * V, f);
-        }
-    }
+    if (t < n_tok && lane == 0) {
+        // gave up on row j: report it, then wait for this warp's copies still
+        // in flight (rows j .. j + RMSB_NBUF - 1) before its shared memory is
+        // released
+        atomicOr(err, 1);
+        for (int i = 0; i < RMSB_NBUF && t + i * stride < n_tok; ++i)
+            mbar_wait(&bar[(j + i) % RMSB_NBUF], ((j + i) / RMSB_NBUF) & 1, nullptr, RMS_DRAIN_NS);
     }
 }
 
@@ -764,8 +850,7 @@ __global__ void splitk_rmsnorm_kernel(const float* __restrict__ part, int nsplit
         store_vec<T>(cr + v * V, a);
     }
     block_sum_pair(hi, lo, red);   // its barriers also order the c stores before the reads below
-    const float ms = static_cast<float>((static_cast<double>(hi) + static_cast<double>(lo)) /
-                                        static_cast<double>(rank));
+    const float ms = mean_of_pair(hi, lo, rank);
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
     for (int v = threadIdx.x; v < rank / V; v += blockDim.x) {
         float f[V], g[V];

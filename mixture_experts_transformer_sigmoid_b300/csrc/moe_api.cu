@@ -427,6 +427,44 @@ int launch_router_tc(moe_handle* h, const void* router_w, const void* xn, int T,
     return cudaGetLastError() == cudaSuccess ? 2 : 0;
 }
 
+// RMSNorm of Tn rows of d elements.  From 8 tokens per SM up, a warp per
+// token with the rows staged in shared memory (rmsnorm_bulk_kernel: as many
+// warps per block, up to RMSB_WARPS_MAX, as fit RMSB_NBUF row buffers each
+// next to the gain row in RMSB_SMEM_BUDGET; as many blocks as are resident
+// at once, each warp looping over tokens); smaller batches, and rows too long
+// for one such warp, a block per token.
+constexpr size_t RMSB_SMEM_BUDGET = 216 * 1024;
+
+template <typename T>
+cudaError_t launch_rmsnorm(moe_handle* h, const T* x, const T* gain, T* xn, int Tn, int d, float eps,
+                           cudaStream_t st) {
+    const size_t row_bytes = static_cast<size_t>(d) * sizeof(T);
+    const size_t fixed = rmsb_smem(0, row_bytes);   // barriers and the gain row
+    const int warps = fixed >= RMSB_SMEM_BUDGET
+                          ? 0
+                          : static_cast<int>(std::min<size_t>(RMSB_WARPS_MAX,
+                                                              (RMSB_SMEM_BUDGET - fixed) / (RMSB_NBUF * row_bytes)));
+    if (Tn < 8 * h->num_sms || warps < 1)
+        return launch_dep(rmsnorm_kernel<T>, Tn, 256, 0, st, x, gain, xn, d, eps);
+    static bool attr_set[64] = {};   // per device: the budget as the kernel's shared-memory limit
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(rmsnorm_bulk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(RMSB_SMEM_BUDGET));
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const size_t smem = rmsb_smem(warps, row_bytes);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rmsnorm_bulk_kernel<T>, 32 * warps, smem);
+    if (e != cudaSuccess) return e;
+    const int blocks = std::min(std::max(per_sm, 1) * h->num_sms, (Tn + warps - 1) / warps);
+    return launch_dep(rmsnorm_bulk_kernel<T>, blocks, 32 * warps, smem, st, x, gain, xn, Tn, d, eps, h->err);
+}
+
 // The fused small-batch routing block, instantiated for the experts per lane.
 template <int EPL>
 cudaError_t launch_route_small_e(const RouteSmallArgs& ra, cudaStream_t st) {
@@ -488,14 +526,8 @@ moe_status forward_simt_or_routing(moe_handle* h, const FwdArgs& a, cudaStream_t
     // A+B: RMSNorm and router logits
     mark(h, 0, st);
     if (h->tc) {
-        // a warp per token once there are enough tokens to fill the SMs; small
-        // batches (decode) keep a whole block on each token
-        if (Tn >= 8 * h->num_sms)
-            launch_dep(rmsnorm_warp_kernel<T>, (Tn + 7) / 8, 256, 0, st,
-                       x, static_cast<const T*>(a.norm_w), xn, Tn, d, c.eps);
-        else
-            launch_dep(rmsnorm_kernel<T>, Tn, 256, 0, st,
-                       x, static_cast<const T*>(a.norm_w), xn, d, c.eps);
+        if (launch_rmsnorm(h, x, static_cast<const T*>(a.norm_w), xn, Tn, d, c.eps, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
         mark(h, 1, st);
         const int n_router = launch_router_tc(h, a.router_w, xn, Tn, st, small ? &ks_left : nullptr);
         if (n_router == 0) return MOE_ERR_CUDA;
@@ -689,12 +721,8 @@ moe_status dense_impl(moe_handle* h, int Tn, const void* x_, const void* norm_w,
     const T* x = static_cast<const T*>(x_);
     T* xn = static_cast<T*>(h->xn);
     T* hd = static_cast<T*>(h->hd);
-    if (Tn >= 8 * h->num_sms)
-        launch_dep(rmsnorm_warp_kernel<T>, (Tn + 7) / 8, 256, 0, st,
-                   x, static_cast<const T*>(norm_w), xn, Tn, d, c.eps);
-    else
-        launch_dep(rmsnorm_kernel<T>, Tn, 256, 0, st,
-                   x, static_cast<const T*>(norm_w), xn, d, c.eps);
+    if (launch_rmsnorm(h, x, static_cast<const T*>(norm_w), xn, Tn, d, c.eps, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
     if (h->tc) {
         // CTA pairs (256 x 256 tiles) from two 64-token tiles up
         const bool pair = Tn >= 128;
@@ -785,17 +813,13 @@ moe_status q_latent_impl(moe_handle* h, int Tn, int rank, const void* hidden, co
     const int d = c.hidden;
     T* cq = static_cast<T*>(c_out);
     auto norm = [&]() {
-        if (Tn >= 8 * h->num_sms)
-            launch_dep(rmsnorm_warp_kernel<T>, (Tn + 7) / 8, 256, 0, st,
-                       cq, static_cast<const T*>(gain), static_cast<T*>(q_out), Tn, rank, c.eps);
-        else
-            launch_dep(rmsnorm_kernel<T>, Tn, 256, 0, st,
-                       cq, static_cast<const T*>(gain), static_cast<T*>(q_out), rank, c.eps);
+        return launch_rmsnorm(h, static_cast<const T*>(cq), static_cast<const T*>(gain), static_cast<T*>(q_out), Tn,
+                              rank, c.eps, st);
     };
     if (!h->tc) {
         simt_shared_down_kernel<T><<<dim3(Tn, (rank + 127) / 128), 128, d * sizeof(float), st>>>(
             static_cast<const T*>(hidden), static_cast<const T*>(w_qa), d, rank, cq);
-        norm();
+        if (norm() != cudaSuccess) return MOE_ERR_CUDA;
         h->launches += 2;
         return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
     }
@@ -814,7 +838,7 @@ moe_status q_latent_impl(moe_handle* h, int Tn, int rank, const void* hidden, co
         g.seg[0] = TcSeg{0, Tn, d, 256, 64, (rank + 255) / 256, rank, rank, c_out, nullptr, 128, PA_ONE_2D};
         set_dense_groups(g.seg[0], 256);
         if (run_tc<EPI_WEIGHTED>(g, true, Tn, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
-        norm();
+        if (norm() != cudaSuccess) return MOE_ERR_CUDA;
         h->launches += 2;
         return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
     }
@@ -838,7 +862,7 @@ moe_status q_latent_impl(moe_handle* h, int Tn, int rank, const void* hidden, co
                    static_cast<T*>(q_out));
     } else {
         if (run_tc<EPI_WEIGHTED>(g, false, Tn, h->num_sms, st) != cudaSuccess) return MOE_ERR_CUDA;
-        norm();
+        if (norm() != cudaSuccess) return MOE_ERR_CUDA;
     }
     h->launches += 2;
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
