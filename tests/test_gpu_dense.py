@@ -36,6 +36,10 @@ SMALL = {
     "dense_single_odd_bf16": DW("dense_single_odd_bf16", T=77, d=320, I=192, dtype="bf16"),
     "dense_one_token_bf16": DW("dense_one_token_bf16", T=1, d=512, I=256, dtype="bf16"),
     "dense_ragged_fp32": DW("dense_ragged_fp32", T=53, d=128, I=96, dtype="fp32"),
+    # prefill-sized batches (at least 8 tokens per SM): the RMSNorm with rows staged in
+    # shared memory, 40 vectors per row (lanes hold one or two), in bf16 and in fp32
+    "dense_prefill_odd_bf16": DW("dense_prefill_odd_bf16", T=1250, d=320, I=192, dtype="bf16"),
+    "dense_prefill_fp32": DW("dense_prefill_fp32", T=1250, d=160, I=96, dtype="fp32"),
 }
 
 

@@ -41,6 +41,10 @@ SMALL = {
     # feature tiles in both GEMMs and a shared expert narrower than one pair tile
     "pair_odd_sizes_bf16": W("pair_odd_sizes_bf16", T=1000, d=320, E=8, I=192, Is=64, k=3,
                              routed_scale=2.5, dtype="bf16"),
+    # a prefill-sized batch (at least 8 tokens per SM) whose rows are 40 vectors: the
+    # RMSNorm with rows staged in shared memory, lanes holding one or two vectors
+    "prefill_norm_odd_bf16": W("prefill_norm_odd_bf16", T=1250, d=320, E=8, I=128, Is=64, k=2,
+                               routed_scale=1.0, dtype="bf16"),
     # every token routed to one hot expert (bias +5): one expert with 1500 rows, six
     # token tiles on the CTA-pair path, the other slot spread over the rest
     "all_hot_expert_bf16": W("all_hot_expert_bf16", T=1500, d=256, E=16, I=128, Is=64, k=2,
